@@ -1,0 +1,171 @@
+"""CPU fp64 oracle for 2-D grouped / depthwise convolution.
+
+TEST INFRASTRUCTURE, not part of the product path: only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import it.  It shares no code with the CUDA library and never imports it.
+
+The arithmetic lives in ``conv_oracle.c`` (plain loops, fp64, OpenMP over
+output planes); this module compiles it with gcc and marshals arrays.  Inputs
+of any dtype are widened to float64 exactly (fp16, bf16 and fp32 all embed in
+fp64) and put in dense logical NCHW order before the call, so the oracle
+reads both memory layouts through one plain index function.
+
+The parity rule it serves (from the workload contract): an element passes when
+|gpu - ref| <= tol * bound + 1e-6, with bound = sum of |w*x| over the taps and
+tol = 1e-5 (fp32), 2e-3 (fp16), 1.6e-2 (bf16).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 1.6e-2}
+ABS_TOL = 1e-6
+
+
+def build(force: bool = False) -> str:
+    """Compile conv_oracle.c into a shared library (OpenMP when available)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+            "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, dp = ctypes.c_int64, ctypes.POINTER(ctypes.c_double)
+            lib.oracle_out_size.restype = i64
+            lib.oracle_out_size.argtypes = [i64] * 5
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_num_threads.argtypes = []
+            common = [dp, dp, dp] + [i64] * 14
+            lib.oracle_conv2d_f64.restype = ctypes.c_int
+            lib.oracle_conv2d_f64.argtypes = common + [dp, dp]
+            lib.oracle_conv2d_f64_points.restype = ctypes.c_int
+            lib.oracle_conv2d_f64_points.argtypes = (
+                common + [i64, ctypes.POINTER(ctypes.c_int64), dp, dp])
+            _lib = lib
+    return _lib
+
+
+def _as_f64(a) -> np.ndarray:
+    """Widen a torch tensor or array to a dense float64 numpy array in
+    logical index order (exact for fp16 / bf16 / fp32)."""
+    if a is None:
+        return None
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().to("cpu", torch.float64).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _pair(v):
+    if isinstance(v, int):
+        return (v, v)
+    v = tuple(int(t) for t in v)
+    assert len(v) == 2
+    return v
+
+
+def out_size(in_size: int, k: int, s: int, pb: int, pa: int) -> int:
+    """Output length along one spatial dim (-1 when the window never fits)."""
+    return int(_load().oracle_out_size(in_size, k, s, pb, pa))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double)) if a is not None else None
+
+
+def _prep(x, w, b, stride, pad_before, pad_after, groups):
+    x = _as_f64(x)
+    w = _as_f64(w)
+    b = _as_f64(b)
+    if x.ndim == 3:
+        x = x[None]
+    if x.ndim != 4 or w.ndim != 4:
+        raise ValueError("x must be [N,C,H,W] (or [C,H,W]); w must be [Co,Cig,KH,KW]")
+    sh, sw = _pair(stride)
+    pbh, pbw = _pair(pad_before)
+    pah, paw = _pair(pad_before if pad_after is None else pad_after)
+    N, C_in, H, W = x.shape
+    C_out, Cin_g, KH, KW = w.shape
+    if Cin_g * groups != C_in:
+        raise ValueError("C_in must equal Cin_g * groups")
+    if b is not None and b.shape != (C_out,):
+        raise ValueError("bias must be [C_out]")
+    OH = out_size(H, KH, sh, pbh, pah)
+    OW = out_size(W, KW, sw, pbw, paw)
+    if OH < 0 or OW < 0:
+        raise ValueError("window larger than the padded input")
+    dims = (N, C_in, H, W, C_out, groups, KH, KW, sh, sw, pbh, pbw, pah, paw)
+    return x, w, b, dims, (N, C_out, OH, OW)
+
+
+def conv2d(x, w, b=None, stride=1, pad_before=0, pad_after=None, groups=1):
+    """Reference convolution.  Returns (y, bound) as float64 arrays of shape
+    [N, C_out, OH, OW]."""
+    x, w, b, dims, oshape = _prep(x, w, b, stride, pad_before, pad_after, groups)
+    y = np.empty(oshape, dtype=np.float64)
+    bound = np.empty(oshape, dtype=np.float64)
+    rc = _load().oracle_conv2d_f64(_ptr(x), _ptr(w), _ptr(b), *dims, _ptr(y), _ptr(bound))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return y, bound
+
+
+def conv2d_points(x, w, b, stride, pad_before, pad_after, groups, pts):
+    """Reference values at selected outputs.  ``pts`` is an [P, 4] integer
+    array of (n, co, oh, ow).  Returns (y, bound), each of length P."""
+    x, w, b, dims, _ = _prep(x, w, b, stride, pad_before, pad_after, groups)
+    pts = np.ascontiguousarray(np.asarray(pts, dtype=np.int64).reshape(-1, 4))
+    y = np.empty(len(pts), dtype=np.float64)
+    bound = np.empty(len(pts), dtype=np.float64)
+    rc = _load().oracle_conv2d_f64_points(
+        _ptr(x), _ptr(w), _ptr(b), *dims, len(pts),
+        pts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _ptr(y), _ptr(bound))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments or a point")
+    return y, bound
+
+
+def violations(got, ref, bound, dtype: str):
+    """Boolean mask of elements outside |got - ref| <= tol*bound + 1e-6."""
+    got = _as_f64(got)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = np.asarray(bound, dtype=np.float64)
+    tol = TOL[dtype]
+    with np.errstate(invalid="ignore"):
+        bad = ~(np.abs(got - ref) <= tol * bound + ABS_TOL)
+    return bad

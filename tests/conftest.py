@@ -1,0 +1,28 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a CUDA GPU (runs the sm_103a kernels through the C ABI)")
+
+
+def pytest_collection_modifyitems(config, items):
+    """A gpu-marked test on a machine without a GPU is a skip, never a pass."""
+    try:
+        import torch
+        have_gpu = torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        have_gpu = False
+    if have_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device on this machine")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)
