@@ -1,0 +1,283 @@
+"""GB300 direct-stencil depthwise / few-channel grouped 2-D convolution.
+
+A thin Python binding over the C ABI in ``include/gconv.h`` (``libgconv.so``,
+hand-written sm_103a CUDA kernels).  This module only marshals arguments:
+every step of the convolution runs in the library's kernels, and there is no
+CPU fallback -- a missing library is an error.
+
+Functions keep the ABI's names: ``conv_bind``, ``out_shape_and_stride``,
+``conv_dw_forward``, ``conv_grouped_forward``, ``conv_select_schedule``,
+``conv_force_schedule``; ``conv2d`` strings them together for torch tensors.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+__all__ = [
+    "build", "conv_bind", "out_shape_and_stride", "conv_dw_forward",
+    "conv_grouped_forward", "conv_select_schedule", "conv_force_schedule",
+    "conv_schedule_name", "conv_strerror", "conv_launch_count", "conv2d",
+    "GconvError", "SCHEDULES", "lib_path",
+]
+
+SCHEDULES = {"auto": -1, "dw_flat": 0, "dw_row8": 1, "dw_mult": 2,
+             "grp_plane": 3, "grp_reduce": 4}
+_DTYPE_CODES = {"float32": 0, "float16": 1, "bfloat16": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GconvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_strerror(status)} (status {status})")
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32), ("sizes", ctypes.c_int64 * 4),
+                ("strides", ctypes.c_int64 * 4)]
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [
+        ("magic", ctypes.c_uint32), ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32),
+        ("has_bias", ctypes.c_int32), ("unbatched", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
+        ("N", ctypes.c_int64), ("C_in", ctypes.c_int64), ("H", ctypes.c_int64),
+        ("W", ctypes.c_int64), ("C_out", ctypes.c_int64), ("groups", ctypes.c_int64),
+        ("Cin_g", ctypes.c_int64), ("Cout_g", ctypes.c_int64), ("KH", ctypes.c_int64),
+        ("KW", ctypes.c_int64), ("OH", ctypes.c_int64), ("OW", ctypes.c_int64),
+        ("stride", ctypes.c_int32 * 2), ("pad_before", ctypes.c_int32 * 2),
+        ("pad_after", ctypes.c_int32 * 2),
+        ("x_strides", ctypes.c_int64 * 4), ("w_strides", ctypes.c_int64 * 4),
+        ("b_stride", ctypes.c_int64), ("y_strides", ctypes.c_int64 * 4),
+        ("x_dense", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
+
+
+def lib_path() -> str:
+    from . import _build
+    return _build.LIB
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libgconv.so for sm_103a (in-tree) and return its path."""
+    from . import _build
+    return _build.build(force=force, verbose=verbose)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build the CUDA library first "
+                "(grouped_convolution_gb300.build()); there is no fallback")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, vp = ctypes.POINTER, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+        lib.conv_bind.restype = i32
+        lib.conv_bind.argtypes = [P(Tensor), P(Tensor), P(Tensor), i32, P(i32), P(i32),
+                                  P(i32), P(i32), i64, P(Desc)]
+        lib.out_shape_and_stride.restype = i32
+        lib.out_shape_and_stride.argtypes = [P(Desc), P(i32), P(i64), P(i64)]
+        for fn in (lib.conv_dw_forward, lib.conv_grouped_forward):
+            fn.restype = i32
+            fn.argtypes = [P(Desc), vp, vp, vp, vp, vp]
+        lib.conv_select_schedule.restype = i32
+        lib.conv_select_schedule.argtypes = [P(Desc), vp, vp, vp, vp, P(i32)]
+        lib.conv_force_schedule.restype = i32
+        lib.conv_force_schedule.argtypes = [i32]
+        lib.conv_schedule_name.restype = ctypes.c_char_p
+        lib.conv_schedule_name.argtypes = [i32]
+        lib.conv_strerror.restype = ctypes.c_char_p
+        lib.conv_strerror.argtypes = [i32]
+        lib.conv_test_inject_launch_error.restype = None
+        lib.conv_test_inject_launch_error.argtypes = [i32]
+        lib.conv_last_cuda_error.restype = i32
+        lib.conv_last_cuda_error.argtypes = []
+        lib.conv_launch_count.restype = ctypes.c_uint64
+        lib.conv_launch_count.argtypes = []
+        lib.conv_version.restype = i32
+        lib.conv_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _strerror(status: int) -> str:
+    try:
+        return _load().conv_strerror(status).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise GconvError(status, what)
+
+
+def _pair(v, name) -> Tuple[int, int]:
+    if isinstance(v, int):
+        return (v, v)
+    v = tuple(int(t) for t in v)
+    if len(v) != 2:
+        raise ValueError(f"{name} must be an int or a pair")
+    return v
+
+
+def geometry(sizes: Sequence[int], strides: Sequence[int]) -> Tensor:
+    t = Tensor()
+    t.rank = len(sizes)
+    # Ranks above 4 keep their rank so the library can reject them.
+    for i, (s, st) in enumerate(list(zip(sizes, strides))[:4]):
+        t.sizes[i] = int(s)
+        t.strides[i] = int(st)
+    return t
+
+
+def _dtype_code(dtype) -> int:
+    name = str(dtype).replace("torch.", "")
+    if name not in _DTYPE_CODES:
+        raise GconvError(3, f"dtype {dtype}")
+    return _DTYPE_CODES[name]
+
+
+def conv_bind(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
+              dilation=1, groups=1, dtype=None) -> Desc:
+    """Validate and canonicalise one convolution.  ``x``, ``w`` and ``bias``
+    may be torch tensors or ``(sizes, strides)`` pairs (then ``dtype`` names
+    the element type).  Returns the ABI's ``gconv_desc``."""
+    def geo(t):
+        if t is None:
+            return None
+        if isinstance(t, tuple):
+            return geometry(*t)
+        return geometry(t.shape, t.stride())
+    if dtype is None:
+        dtype = x.dtype
+        for t in (w, bias):
+            if t is not None and not isinstance(t, tuple) and t.dtype != dtype:
+                raise GconvError(3, "x, w and bias must share one dtype")
+    xs, ws, bs = geo(x), geo(w), geo(bias)
+    arr = ctypes.c_int32 * 2
+    st = arr(*_pair(stride, "stride"))
+    pb = arr(*_pair(padding_before, "padding_before"))
+    pa = arr(*_pair(padding_before if padding_after is None else padding_after,
+                    "padding_after"))
+    dl = arr(*_pair(dilation, "dilation"))
+    d = Desc()
+    rc = _load().conv_bind(ctypes.byref(xs), ctypes.byref(ws),
+                           ctypes.byref(bs) if bs is not None else None,
+                           _dtype_code(dtype), st, pb, pa, dl, int(groups), ctypes.byref(d))
+    _check(rc, "conv_bind")
+    return d
+
+
+def out_shape_and_stride(desc: Desc):
+    """Output (sizes, strides) in elements, as the ABI computes them."""
+    rank = ctypes.c_int32()
+    sizes = (ctypes.c_int64 * 4)()
+    strides = (ctypes.c_int64 * 4)()
+    _check(_load().out_shape_and_stride(ctypes.byref(desc), ctypes.byref(rank), sizes, strides),
+           "out_shape_and_stride")
+    r = rank.value
+    return tuple(sizes[:r]), tuple(strides[:r])
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def conv_dw_forward(desc: Desc, x, w, bias, y, stream=None):
+    """Depthwise forward into the preallocated ``y`` (device tensors or raw
+    device pointers), on ``stream`` (default: torch's current stream)."""
+    _check(_load().conv_dw_forward(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias),
+                                   _ptr(y), _stream_ptr(stream)), "conv_dw_forward")
+
+
+def conv_grouped_forward(desc: Desc, x, w, bias, y, stream=None):
+    """Grouped forward (1..8 input channels per group) into ``y``."""
+    _check(_load().conv_grouped_forward(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias),
+                                        _ptr(y), _stream_ptr(stream)), "conv_grouped_forward")
+
+
+def conv_select_schedule(desc: Desc, x, w, bias, y) -> str:
+    """Name of the schedule a forward call would run (no launch)."""
+    out = ctypes.c_int32()
+    _check(_load().conv_select_schedule(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias),
+                                        _ptr(y), ctypes.byref(out)), "conv_select_schedule")
+    return conv_schedule_name(out.value)
+
+
+def conv_force_schedule(schedule) -> None:
+    """Process-wide override: a schedule name, number, or "auto"/None."""
+    if schedule is None:
+        schedule = -1
+    if isinstance(schedule, str):
+        if schedule not in SCHEDULES:
+            raise GconvError(11, f"schedule {schedule!r}")
+        schedule = SCHEDULES[schedule]
+    _check(_load().conv_force_schedule(int(schedule)), "conv_force_schedule")
+
+
+def conv_schedule_name(schedule: int) -> str:
+    return _load().conv_schedule_name(int(schedule)).decode()
+
+
+def conv_strerror(status: int) -> str:
+    return _strerror(status)
+
+
+def conv_launch_count() -> int:
+    return int(_load().conv_launch_count())
+
+
+def conv_test_inject_launch_error(cuda_error: int) -> None:
+    _load().conv_test_inject_launch_error(int(cuda_error))
+
+
+def conv_last_cuda_error() -> int:
+    return int(_load().conv_last_cuda_error())
+
+
+def empty_output(desc: Desc, like):
+    """Allocate y (torch) with exactly the sizes and strides the ABI gives."""
+    import torch
+    sizes, strides = out_shape_and_stride(desc)
+    return torch.empty_strided(sizes, strides, dtype=like.dtype, device=like.device)
+
+
+def conv2d(x, w, bias=None, stride=1, padding_before=0, padding_after=None, groups=1,
+           schedule=None, out=None, stream=None):
+    """Bind, allocate the output and run the forward on CUDA tensors."""
+    if not (x.is_cuda and w.is_cuda and (bias is None or bias.is_cuda)):
+        raise GconvError(1, "conv2d needs CUDA tensors (there is no CPU path)")
+    d = conv_bind(x, w, bias, stride, padding_before, padding_after, 1, groups)
+    if schedule is not None:
+        d.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
+    y = empty_output(d, x) if out is None else out
+    if d.Cin_g == 1:
+        conv_dw_forward(d, x, w, bias, y, stream)
+    else:
+        conv_grouped_forward(d, x, w, bias, y, stream)
+    return y

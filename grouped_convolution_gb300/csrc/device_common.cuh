@@ -1,0 +1,75 @@
+// device_common.cuh -- element conversions and small helpers shared by the
+// kernels.  All arithmetic is fp32; inputs are widened exactly and the result
+// is rounded once, to nearest even, by the hardware conversion.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace gconv {
+
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
+    static __device__ __forceinline__ float to_f32(float v) { return v; }
+    static __device__ __forceinline__ float from_f32(float v) { return v; }
+};
+
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float load(const __half *p) { return __half2float(__ldg(p)); }
+    static __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ __half from_f32(float v) { return __float2half_rn(v); }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(__ldg(p));
+    }
+    static __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f32(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Widen the two 16-bit values packed in a 32-bit word (low half first).
+__device__ __forceinline__ float2 unpack2(uint32_t v, __nv_bfloat16 *) {
+    // bf16 -> fp32 is exact: the 16 bits become the top half of the word.
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+__device__ __forceinline__ float2 unpack2(uint32_t v, __half *) {
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    return __half22float2(h);
+}
+__device__ __forceinline__ float2 unpack2(uint32_t v, float *) {
+    return make_float2(0.f, 0.f);  // not used for fp32
+}
+
+// Round two fp32 values to one packed 32-bit word (low half first).
+__device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16 *) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, __half *) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const T *p) { return Elem<T>::load(p); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v) { return Elem<T>::from_f32(v); }
+
+}  // namespace gconv
+
+// Dispatch a templated launcher on the runtime dtype code.
+#define GCONV_DISPATCH_DTYPE(dt, T, ...)                            \
+    [&]() -> cudaError_t {                                          \
+        switch (dt) {                                               \
+        case GCONV_F32: { using T = float; return __VA_ARGS__(); }  \
+        case GCONV_F16: { using T = __half; return __VA_ARGS__(); } \
+        case GCONV_BF16: { using T = __nv_bfloat16; return __VA_ARGS__(); } \
+        }                                                           \
+        return cudaErrorInvalidValue;                               \
+    }()

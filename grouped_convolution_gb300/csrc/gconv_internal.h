@@ -1,0 +1,56 @@
+// gconv_internal.h -- shared declarations between the host library and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gconv.h"
+
+namespace gconv {
+
+constexpr uint32_t kDescMagic = 0x47434f4eu;  // "GCON"
+
+// Everything a kernel needs, by value.  Spatial and channel extents are
+// checked by conv_bind to fit in int32; strides stay 64-bit.
+struct Params {
+    int N, C_in, H, W, C_out, G, Cin_g, Cout_g, KH, KW, OH, OW;
+    int sh, sw, pbh, pbw;
+    int has_bias, layout, dtype;
+    int64_t xs[4];   // x strides, logical (N, C, H, W)
+    int64_t ws[4];   // w strides, logical (C_out, Cin_g, KH, KW)
+    int64_t bs;      // bias stride
+    int64_t ys[4];   // y strides, logical (N, C_out, OH, OW)
+};
+
+struct Ptrs {
+    const void *x;
+    const void *w;
+    const void *b;   // nullptr when there is no bias
+    void *y;
+};
+
+Params make_params(const gconv_desc &d);
+
+// One launcher per schedule.  `supports` is pure host logic (shape, layout,
+// alignment); `launch` enqueues the kernel(s) and returns the launch count.
+struct Schedule {
+    const char *name;
+    bool (*supports)(const gconv_desc &d, const Ptrs &p);
+    cudaError_t (*launch)(const Params &pr, const Ptrs &p, cudaStream_t s, int *launches);
+};
+
+// Schedules, indexed by gconv_schedule.
+extern const Schedule kDwFlat;
+extern const Schedule kDwRow8;
+extern const Schedule kDwMult;
+extern const Schedule kGrpPlane;
+extern const Schedule kGrpReduce;
+
+inline bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+inline int dtype_size(int dt) { return dt == GCONV_F32 ? 4 : 2; }
+
+}  // namespace gconv

@@ -1,0 +1,220 @@
+/*
+ * gconv.h -- C ABI of the GB300 direct-stencil convolution library.
+ *
+ * One operation: 2-D depthwise and few-channel grouped convolution
+ * (cross-correlation, zero padding, dilation 1) with
+ *   - groups of 1..8 input channels and any number of output channels each
+ *     (any depthwise channel multiplier),
+ *   - kernels from 1x1 to 9x9 (KH and KW independent), any stride >= 1,
+ *   - explicit, possibly asymmetric, padding before and after each spatial dim,
+ *   - fp32, fp16 or bf16 tensors (all of one dtype), fp32 accumulation and a
+ *     single round-to-nearest-even cast of (sum + bias) at the end,
+ *   - NCHW- or channels-last-ordered input, optional bias.
+ * The envelope is the one of the direct-stencil template in executorch PR
+ * #25085 "Route 2-D depthwise and few-channel grouped convolutions to a
+ * Triton direct-stencil kernel" (description, second paragraph).
+ *
+ * Semantics.  For output (n, co, oh, ow), with g = co / Cout_g:
+ *   y = b[co] + sum_{ci, kh, kw} w[co, ci, kh, kw] * x[n, g*Cin_g + ci, ih, iw],
+ *   ih = oh*stride_h - pad_before_h + kh,  iw = ow*stride_w - pad_before_w + kw,
+ * where taps with (ih, iw) outside the input contribute zero.  The tap
+ * indexing is the one of torch/_inductor/kernel/conv.py, LOOP_BODY_2D; the
+ * channel-to-group mapping that of conv2d_template in the same file; the
+ * explicit padding_before / padding_after pair that of the canonical
+ * convolution op in executorch PR #25084 "Add triton::convolution and the conv
+ * routing framework" (description, second paragraph).
+ *
+ * Call sequence (PR #25084, second paragraph: the arguments are bound and
+ * validated once, the output layout is computed by one function, the output
+ * is allocated once by the caller and the kernels only write into it):
+ *   conv_bind -> out_shape_and_stride -> caller allocates y ->
+ *   conv_dw_forward (Cin_g == 1) or conv_grouped_forward (1 <= Cin_g <= 8).
+ *
+ * Ownership.  The caller owns every buffer.  The library allocates no memory
+ * (no workspace), keeps no pointer after a call returns and never
+ * synchronises; kernels run asynchronously on the caller's stream.
+ *
+ * Errors.  Every entry point returns a gconv_status; nothing throws or
+ * aborts across the ABI.  conv_strerror() names a status.
+ *
+ * Threads.  All entry points are re-entrant.  The process-wide schedule
+ * override (conv_force_schedule) and the injected-error hook are atomics.
+ */
+#ifndef GCONV_H
+#define GCONV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t / CUstream).
+ * NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *gconv_stream;
+
+typedef enum gconv_dtype {
+    GCONV_F32 = 0,
+    GCONV_F16 = 1,
+    GCONV_BF16 = 2
+} gconv_dtype;
+
+typedef enum gconv_status {
+    GCONV_OK = 0,
+    GCONV_ERR_NULL = 1,          /* a required pointer is NULL, or bias presence mismatches */
+    GCONV_ERR_RANK = 2,          /* x not rank 3/4, w not rank 4, bias not rank 1 */
+    GCONV_ERR_DTYPE = 3,         /* unknown dtype code */
+    GCONV_ERR_SHAPE = 4,         /* channel/group/weight/bias size mismatch, stride < 1, negative size */
+    GCONV_ERR_UNSUPPORTED = 5,   /* dilation != 1, KH or KW outside [1, 9], Cin_g > 8,
+                                    Cin_g != 1 on conv_dw_forward */
+    GCONV_ERR_PADDING = 6,       /* negative padding, or the window never fits the padded input */
+    GCONV_ERR_ALIGN = 7,         /* a forced schedule needs alignment the pointers lack */
+    GCONV_ERR_CUDA = 8,          /* a CUDA launch failed (cudaGetLastError after the launch) */
+    GCONV_ERR_INTERNAL = 9,      /* descriptor not produced by conv_bind, or a size overflow */
+    GCONV_ERR_LAYOUT = 10,       /* x is neither NCHW- nor channels-last-ordered */
+    GCONV_ERR_SCHEDULE = 11      /* a forced schedule does not support this call */
+} gconv_status;
+
+/* The five schedules of the direct-stencil template (PR #25085, second
+ * paragraph), re-designed for sm_103a.  GCONV_SCHED_AUTO lets the per-shape
+ * picker choose. */
+typedef enum gconv_schedule {
+    GCONV_SCHED_AUTO = -1,
+    GCONV_SCHED_DW_FLAT = 0,     /* portable base: any layout, multiplier and group shape */
+    GCONV_SCHED_DW_ROW8 = 1,     /* channels-last depthwise: 16-byte channel vectors,
+                                    register sliding window down the rows */
+    GCONV_SCHED_DW_MULT = 2,     /* depthwise, multiplier <= 16: every output channel of an
+                                    input channel from one input load */
+    GCONV_SCHED_GRP_PLANE = 3,   /* grouped: a block per (image, group, tile), the group's
+                                    weights shared in shared memory */
+    GCONV_SCHED_GRP_REDUCE = 4,  /* grouped, few outputs: taps split across the lanes of a
+                                    warp and reduced with shuffles */
+    GCONV_SCHED_COUNT = 5
+} gconv_schedule;
+
+typedef enum gconv_layout {
+    GCONV_LAYOUT_NCHW = 0,
+    GCONV_LAYOUT_NHWC = 1        /* channels-last */
+} gconv_layout;
+
+/* A tensor's geometry: logical sizes and element strides.  x is [N, C, H, W]
+ * (or [C, H, W] when unbatched), w is [C_out, C_in/groups, KH, KW], bias is
+ * [C_out].  Strides are in elements, in the same logical order. */
+typedef struct gconv_tensor {
+    int32_t rank;
+    int64_t sizes[4];
+    int64_t strides[4];
+} gconv_tensor;
+
+/* The canonical, validated description of one convolution, filled by
+ * conv_bind.  Callers may change only `schedule` (GCONV_SCHED_AUTO or a
+ * gconv_schedule value to force one schedule for calls with this desc). */
+typedef struct gconv_desc {
+    uint32_t magic;              /* set by conv_bind */
+    int32_t dtype;               /* gconv_dtype */
+    int32_t layout;              /* gconv_layout of x; y uses the same */
+    int32_t has_bias;
+    int32_t unbatched;           /* x was rank 3: y is rank 3 too */
+    int32_t schedule;            /* GCONV_SCHED_AUTO unless forced by the caller */
+    int64_t N, C_in, H, W;
+    int64_t C_out, groups, Cin_g, Cout_g;
+    int64_t KH, KW, OH, OW;
+    int32_t stride[2];           /* (h, w) */
+    int32_t pad_before[2];       /* (h, w) */
+    int32_t pad_after[2];        /* (h, w) */
+    int64_t x_strides[4];        /* elements, logical (N, C, H, W) order */
+    int64_t w_strides[4];        /* elements, logical (C_out, Cin_g, KH, KW) order */
+    int64_t b_stride;            /* elements; 0 when there is no bias */
+    int64_t y_strides[4];        /* dense in `layout`, logical (N, C_out, OH, OW) order */
+    int32_t x_dense;             /* x is dense (no gaps) in its layout */
+    int32_t reserved;
+} gconv_desc;
+
+/* Validate the arguments of one convolution and canonicalise them into *out
+ * (the binding step of PR #25084, second paragraph: defaults filled, rank-3
+ * input treated as one image -- torch/_inductor/kernel/conv.py, convolution,
+ * adds the batch dim the same way -- and the group shape checked as
+ * C_in == Cin_g * groups).
+ *   x, w:        required geometries; bias: NULL for no bias.
+ *   dtype:       gconv_dtype shared by x, w, bias and y.
+ *   stride, padding_before, padding_after, dilation: (h, w) pairs; NULL
+ *                stride/dilation mean 1, NULL paddings mean 0.
+ *   groups:      >= 1, divides C_in and C_out.
+ * x must be NCHW-ordered (W stride 1, then H, then C, then N, no overlap) or
+ * channels-last-ordered (C stride 1, then W, then H, then N); dims of size 1
+ * are ignored, and when both orders fit NCHW is taken.  Pure host code: no
+ * CUDA call.  Returns GCONV_OK or the first violated rule's status. */
+gconv_status conv_bind(const gconv_tensor *x, const gconv_tensor *w,
+                       const gconv_tensor *bias, int32_t dtype,
+                       const int32_t stride[2], const int32_t padding_before[2],
+                       const int32_t padding_after[2], const int32_t dilation[2],
+                       int64_t groups, gconv_desc *out);
+
+/* The output's rank, sizes and element strides (PR #25084, second paragraph:
+ * one function decides the output layout and both the op and its shape-only
+ * variant use it).  OH = floor((H + pad_before_h + pad_after_h - KH) /
+ * stride_h) + 1 and likewise OW; y is dense in the layout of x
+ * (NCHW in -> NCHW out, channels-last in -> channels-last out) and rank 3
+ * when x was rank 3.  Pure host code. */
+gconv_status out_shape_and_stride(const gconv_desc *d, int32_t *rank,
+                                  int64_t sizes[4], int64_t strides[4]);
+
+/* Depthwise forward (Cin_g == 1, any multiplier C_out / C_in).  x, w, bias
+ * and y are device pointers laid out as the geometries given to conv_bind
+ * and as out_shape_and_stride says for y; bias must be NULL exactly when the
+ * desc has none.  Launches on `stream` and returns without waiting.  Empty
+ * problems (N, C_out, OH or OW zero) return GCONV_OK without a launch.
+ * Returns GCONV_ERR_UNSUPPORTED when Cin_g != 1. */
+gconv_status conv_dw_forward(const gconv_desc *d, const void *x, const void *w,
+                             const void *bias, void *y, gconv_stream stream);
+
+/* Grouped forward (1 <= Cin_g <= 8, any Cout_g); accepts depthwise descs
+ * too.  Same pointer, stream and error contract as conv_dw_forward. */
+gconv_status conv_grouped_forward(const gconv_desc *d, const void *x,
+                                  const void *w, const void *bias, void *y,
+                                  gconv_stream stream);
+
+/* Which schedule a forward call with this desc and these pointers would run
+ * (the picker, or the forced schedule), without launching anything.  Pointer
+ * values are only inspected for alignment.  Returns GCONV_ERR_SCHEDULE /
+ * GCONV_ERR_ALIGN when a forced schedule cannot run the call. */
+gconv_status conv_select_schedule(const gconv_desc *d, const void *x,
+                                  const void *w, const void *bias,
+                                  const void *y, int32_t *schedule);
+
+/* Process-wide override for tests (the force_conv_candidate hook of PR
+ * #25084): every later call whose desc has schedule == GCONV_SCHED_AUTO runs
+ * `schedule`, or the picker again when GCONV_SCHED_AUTO.  The environment
+ * variable GCONV_FORCE_SCHEDULE (a schedule name or number) sets the initial
+ * value.  Returns GCONV_ERR_SCHEDULE for an unknown value. */
+gconv_status conv_force_schedule(int32_t schedule);
+
+/* Name of a schedule ("dw_flat", ...), or "auto" / "unknown". */
+const char *conv_schedule_name(int32_t schedule);
+
+/* Human-readable text for a status. */
+const char *conv_strerror(gconv_status status);
+
+/* Test hook for the failure path: when `cuda_error` is non-zero, the next
+ * forward call that would launch returns GCONV_ERR_CUDA without launching,
+ * exactly as if the launch had failed with that error; 0 clears it.  Lets the
+ * error path be tested without making a GPU fail. */
+void conv_test_inject_launch_error(int32_t cuda_error);
+
+/* The CUDA error code behind the last GCONV_ERR_CUDA returned on this host
+ * thread (0 if none). */
+int32_t conv_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process (all
+ * threads).  Lets callers count launches inside a timed region. */
+uint64_t conv_launch_count(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t conv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCONV_H */
