@@ -11,8 +11,11 @@ fp64) and put in dense logical NCHW order before the call, so the oracle
 reads both memory layouts through one plain index function.
 
 The parity rule it serves (from the workload contract): an element passes when
-|gpu - ref| <= tol * bound + 1e-6, with bound = sum of |w*x| over the taps and
-tol = 1e-5 (fp32), 2e-3 (fp16), 1.6e-2 (bf16).
+|gpu - ref| <= tol * bound + 1e-6, with bound = sum of |w*x| over the taps
+plus |bias| (the bias taken as one more product, bias * 1) and
+tol = 1e-5 (fp32), 2e-3 (fp16), 1.6e-2 (bf16).  Because every tol is above
+half the rounding unit of its dtype and |ref| <= bound, the correctly rounded
+exact result always passes.
 """
 
 from __future__ import annotations

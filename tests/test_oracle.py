@@ -56,6 +56,7 @@ def im2col_conv(x, w, b, stride, pb, pa, groups):
             N, OH, OW, Cog).transpose(0, 3, 1, 2)
     if b is not None:
         y = y + b[None, :, None, None]
+        yabs = yabs + np.abs(b)[None, :, None, None]
     return y, yabs
 
 
@@ -292,6 +293,19 @@ def test_unbatched_and_rejections():
         oracle.conv2d(x, w, None, 1, 0, 0, 3)        # C_in not divisible
     with pytest.raises(ValueError):
         oracle.conv2d(x[:, :2, :2], w, None, 1, 0, 0, 2)  # window > input
+
+
+def test_correct_rounding_always_passes():
+    # Bias-dominated outputs: the exact value rounded to the output dtype
+    # must be inside the tolerance (|ref| <= bound and tol > half an ulp).
+    r = rng(31)
+    x = r.standard_normal((1, 64, 6, 6)) * 1e-3
+    w = r.standard_normal((64, 1, 1, 1)) * 1e-2
+    b = r.uniform(-0.1, 0.1, 64)
+    ref, bound = oracle.conv2d(x, w, b, 1, 0, 0, 64)
+    for name, dt in (("f32", torch.float32), ("f16", torch.float16), ("bf16", torch.bfloat16)):
+        rounded = torch.from_numpy(ref).to(dt)
+        assert not oracle.violations(rounded, ref, bound, name).any()
 
 
 def test_tolerance_rule():
