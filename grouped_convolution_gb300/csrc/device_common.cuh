@@ -41,9 +41,6 @@ __device__ __forceinline__ float2 unpack2(uint32_t v, __half *) {
     __half2 h = *reinterpret_cast<__half2 *>(&v);
     return __half22float2(h);
 }
-__device__ __forceinline__ float2 unpack2(uint32_t v, float *) {
-    return make_float2(0.f, 0.f);  // not used for fp32
-}
 
 // Round two fp32 values to one packed 32-bit word (low half first).
 __device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16 *) {

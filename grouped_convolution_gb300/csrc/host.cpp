@@ -252,10 +252,16 @@ static gconv_status select_impl(const gconv_desc *d, const Ptrs &p, int32_t *out
     return GCONV_OK;
 }
 
+static bool empty_problem(const gconv_desc *d) {
+    return d->N == 0 || d->C_out == 0 || d->OH == 0 || d->OW == 0;
+}
+
 static gconv_status check_call(const gconv_desc *d, const void *x, const void *w,
                                const void *bias, void *y) {
     if (!d) return GCONV_ERR_NULL;
     if (d->magic != kDescMagic) return GCONV_ERR_INTERNAL;
+    // An empty problem touches no memory: its tensors may have NULL data.
+    if (empty_problem(d)) return GCONV_OK;
     if (!x || !w || !y) return GCONV_ERR_NULL;
     if ((bias != nullptr) != (d->has_bias != 0)) return GCONV_ERR_NULL;
     return GCONV_OK;
@@ -274,7 +280,7 @@ static gconv_status forward(const gconv_desc *d, const void *x, const void *w,
                             const void *bias, void *y, gconv_stream stream) {
     gconv_status st = check_call(d, x, w, bias, y);
     if (st != GCONV_OK) return st;
-    if (d->N == 0 || d->C_out == 0 || d->OH == 0 || d->OW == 0) return GCONV_OK;
+    if (empty_problem(d)) return GCONV_OK;
     Ptrs p{x, w, bias, y};
     int32_t s;
     st = select_impl(d, p, &s);

@@ -6,7 +6,6 @@ namespace {
 bool no(const gconv_desc &, const Ptrs &) { return false; }
 cudaError_t none(const Params &, const Ptrs &, cudaStream_t, int *) { return cudaErrorNotSupported; }
 }  // namespace
-const Schedule kDwRow8 = {"dw_row8", no, none};
 const Schedule kDwMult = {"dw_mult", no, none};
 const Schedule kGrpPlane = {"grp_plane", no, none};
 const Schedule kGrpReduce = {"grp_reduce", no, none};

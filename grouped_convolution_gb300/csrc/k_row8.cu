@@ -1,0 +1,47 @@
+// k_row8.cu -- the dw_row8 schedule: which calls it takes and its launcher.
+// The kernel is in k_row8.cuh.
+#include "k_row8.cuh"
+
+namespace gconv {
+namespace {
+
+bool row8_supports(const gconv_desc &d, const Ptrs &q) {
+    if (d.Cin_g != 1 || d.Cout_g != 1) return false;          // multiplier 1
+    if (d.layout != GCONV_LAYOUT_NHWC) return false;          // channel-contiguous
+    if (d.KH != d.KW) return false;
+    if (d.KH != 3 && d.KH != 5 && d.KH != 7) return false;
+    if (d.stride[0] != 1 && d.stride[0] != 2) return false;
+    if (d.stride[1] != d.stride[0]) return false;             // square strides
+    const int es = dtype_size(d.dtype);
+    const int vec = d.dtype == GCONV_F32 ? row8_vec<float>((int)d.KH) : row8_vec<__half>((int)d.KH);
+    if (d.C_out % vec != 0) return false;
+    // 16-byte copies of whole pixels: every pixel run starts on 16 bytes.
+    if (!aligned(q.x, 16)) return false;
+    if ((d.x_strides[0] * es) % 16 || (d.x_strides[2] * es) % 16 || (d.x_strides[3] * es) % 16)
+        return false;
+    // vector stores
+    if (!aligned(q.y, (uintptr_t)(vec * es))) return false;
+    Params p = make_params(d);
+    switch (d.dtype) {
+    case GCONV_F32: return row8_fits_dtype<float>(p);
+    case GCONV_F16: return row8_fits_dtype<__half>(p);
+    case GCONV_BF16: return row8_fits_dtype<__nv_bfloat16>(p);
+    }
+    return false;
+}
+
+cudaError_t row8_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *launches) {
+    *launches = 1;
+    switch (p.dtype) {
+    case GCONV_F32: return row8_launch_f32(p, q, s);
+    case GCONV_F16: return row8_launch_f16(p, q, s);
+    case GCONV_BF16: return row8_launch_bf16(p, q, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+const Schedule kDwRow8 = {"dw_row8", row8_supports, row8_launch};
+
+}  // namespace gconv

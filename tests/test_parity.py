@@ -215,12 +215,11 @@ def test_non_dense_input_and_strided_weights(schedule):
     x, w, b = make_inputs(wl)
     wide = torch.randn(2, 32, 10, 11).to(torch.bfloat16).contiguous(memory_format=torch.channels_last)
     wide[:, 8:24] = x
-    xs = wide[:, 8:24]
     wperm = w.permute(0, 2, 3, 1).contiguous().permute(0, 3, 1, 2)
     bwide = torch.zeros(32, dtype=b.dtype)
     bwide[::2] = b
     dev = torch.device("cuda")
-    xd, wd, bd = xs.to(dev), wperm.to(dev), bwide.to(dev)[::2]
+    xd, wd, bd = wide.to(dev)[:, 8:24], wperm.to(dev), bwide.to(dev)[::2]
     d = gc.conv_bind(xd, wd, bd, 1, 1, 1, 1, 16)
     assert d.x_dense == 0 and d.layout == 1
     d.schedule = gc.SCHEDULES[schedule]
