@@ -224,11 +224,16 @@ gconv_status out_shape_and_stride(const gconv_desc *d, int32_t *rank,
 }
 
 // The per-shape picker.  Specialised schedules win where they apply; the
-// portable base takes everything else.
+// portable base takes everything else.  Calls with too few outputs to give
+// every thread of the GPU its own (fewer than 152 SMs x 512) and a long tap
+// loop split the taps across lanes instead.
 static int32_t pick(const gconv_desc &d, const Ptrs &p) {
     const bool dw = d.Cin_g == 1;
     if (dw && d.Cout_g == 1 && kDwRow8.supports(d, p)) return GCONV_SCHED_DW_ROW8;
     if (dw && kDwMult.supports(d, p)) return GCONV_SCHED_DW_MULT;
+    const double outputs = (double)d.N * d.C_out * d.OH * d.OW;
+    const int64_t taps = d.Cin_g * d.KH * d.KW;
+    if (outputs < 152.0 * 512 && taps >= 32) return GCONV_SCHED_GRP_REDUCE;
     if (kGrpPlane.supports(d, p)) return GCONV_SCHED_GRP_PLANE;
     return GCONV_SCHED_DW_FLAT;
 }
