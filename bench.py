@@ -50,7 +50,30 @@ def parse():
                     help="skip the per-workload breakdown")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--case", default=None,
+                    help="profiling helper: run this workload --reps times and exit (no timing)")
+    ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--schedule", default=None, help="force a schedule for --case")
     return ap.parse_args()
+
+
+def run_case(args):
+    """Run one workload a few times through the C ABI, for ncu captures."""
+    import torch
+    import grouped_convolution_gb300 as gc
+    from grouped_convolution_gb300.inputs import WORKLOADS, make_inputs
+    gc.build()
+    wl = WORKLOADS[args.case]
+    x, w, b = make_inputs(wl, device="cuda")
+    for _ in range(args.reps):
+        y = gc.conv2d(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.groups,
+                      schedule=args.schedule)
+    torch.cuda.synchronize()
+    d = gc.conv_bind(x, w, b, wl.stride, wl.pad_before, wl.pad_after, 1, wl.groups)
+    if args.schedule:
+        d.schedule = gc.SCHEDULES[args.schedule]
+    print(json.dumps({"case": args.case, "reps": args.reps, "shape": list(y.shape),
+                      "schedule": gc.conv_select_schedule(d, x, w, b, y)}))
 
 
 # ------------------------------------------------------------------ helpers
@@ -152,16 +175,30 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def kernel_source_sha(name):
-    path = os.path.join(ROOT, "grouped_convolution_gb300", "csrc", name)
-    try:
-        with open(path, "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
-    except OSError:
-        return None
+# Source files that define each schedule's kernel; the recorded DRAM traffic
+# of a kernel is void once any of them changes.
+KERNEL_SOURCES = {
+    "dw_row8": ["k_row8.cuh", "k_row8.cu", "stencil_math.cuh", "device_common.cuh"],
+    "dw_flat": ["k_flat.cu", "device_common.cuh"],
+    "dw_mult": ["k_mult.cu", "device_common.cuh"],
+    "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh"],
+    "grp_reduce": ["k_reduce.cu", "device_common.cuh"],
+}
 
 
-def recorded_traffic(kernel_file, workload):
+def kernel_source_sha(schedule):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES.get(schedule, []):
+        path = os.path.join(ROOT, "grouped_convolution_gb300", "csrc", name)
+        try:
+            with open(path, "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(schedule, workload):
     """DRAM bytes per launch from the committed ncu summary, if the kernel
     source has not changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -171,7 +208,8 @@ def recorded_traffic(kernel_file, workload):
     except (OSError, ValueError):
         return None
     ent = table.get(workload)
-    if not ent or ent.get("source_sha") != kernel_source_sha(kernel_file):
+    if not ent or ent.get("schedule") != schedule or \
+            ent.get("source_sha") != kernel_source_sha(schedule):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -335,9 +373,7 @@ def run_ours(args):
     dom = cases[0]
     dom_ms = per_kernel[dom.wl.name]
     achieved = dom.bytes / (dom_ms * 1e-3) / 1e9
-    kernel_file = {"dw_row8": "k_row8.cu", "dw_flat": "k_flat.cu", "dw_mult": "k_mult.cu",
-                   "grp_plane": "k_grp.cu", "grp_reduce": "k_grp.cu"}.get(dom.schedule)
-    traffic = recorded_traffic(kernel_file, dom.wl.name) if kernel_file else None
+    traffic = recorded_traffic(dom.schedule, dom.wl.name)
 
     e2e_steps = max(1, min(args.steps, 50))
     e2e_ms, h2d, d2h = time_e2e(cases, e2e_steps, world)
@@ -497,7 +533,9 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.case:
+        run_case(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)
