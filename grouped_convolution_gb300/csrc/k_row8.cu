@@ -15,7 +15,8 @@ bool row8_supports(const gconv_desc &d, const Ptrs &q) {
     const int es = dtype_size(d.dtype);
     const int vec = d.dtype == GCONV_F32 ? row8_vec<float>((int)d.KH) : row8_vec<__half>((int)d.KH);
     if (d.C_out % vec != 0) return false;
-    // 16-byte copies of whole pixels: every pixel run starts on 16 bytes.
+    // TMA: 16-byte aligned base, strides in 16-byte units, the channel
+    // dim contiguous (channels-last order guarantees it).
     if (!aligned(q.x, 16)) return false;
     if ((d.x_strides[0] * es) % 16 || (d.x_strides[2] * es) % 16 || (d.x_strides[3] * es) % 16)
         return false;

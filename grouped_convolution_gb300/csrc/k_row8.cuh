@@ -9,27 +9,33 @@
 //    within one.  A run is a maximal range of those rows with one
 //    (n, cc, hc); rows oh_a..oh_b of a run read the consecutive input rows
 //    oh_a*S_H - pad .. oh_b*S_H - pad + KH - 1, each exactly once.
-//  - Input rows stream through a ring of NS shared-memory stages with
-//    16-byte cp.async copies issued by all threads; zero-fill supplies the
-//    padding, so no bounds test remains in the arithmetic.  NS - 1 rows are
-//    in flight; one block barrier per input row both publishes the row and
-//    frees the stage read one row earlier, which is refilled at once.
+//  - Input rows stream through a ring of NS shared-memory stages filled by
+//    TMA: one thread arms a stage's mbarrier and issues a tiled bulk copy of
+//    the row segment (Win pixels x the chunk's channels); the tensor map's
+//    out-of-bounds zero fill supplies the padding.  NS rows are in flight;
+//    one block barrier per input row frees the stage just read, which the
+//    same thread refills at once.  Consumers wait on the stage's barrier
+//    phase with a bounded poll.
 //  - Thread (cv, pg) owns VEC consecutive channels and S consecutive output
 //    pixels.  Its KH*KW weights (fp32 channel pairs) stay in registers for
 //    the CTA's lifetime.  Each staged input row is widened once into a
-//    window of (S-1)*S_W + KW vectors and multiplied into every output row
-//    still open on it: R = ceil(KH / S_H) accumulator sets rotate through
-//    the output rows, with set indices fixed at compile time by unrolling
-//    the row loop over one rotation period.
+//    window of (S-1)*S_W + KW vectors (32-bit shared addressing) and
+//    multiplied into every output row still open on it: R = ceil(KH / S_H)
+//    accumulator sets rotate through the output rows, with set indices fixed
+//    at compile time by unrolling the row loop over one rotation period.
 //  - Accumulators start at the bias (fp32); a finished output row is
 //    rounded once to the output dtype and stored with coalesced 4/8/16-byte
-//    stores.
-//  - No spin waits: the only waits are cp.async.wait_group on the thread's
-//    own copies and block barriers.
+//    stores through a pointer that advances one output row at a time.
+//  - A wait that gives up (it should never happen) marks the CTA failed;
+//    from then on its outputs are written as NaN, so the failure is visible
+//    in the result instead of hanging the GPU.
 #pragma once
 
 #include "gconv_internal.h"
 #include "stencil_math.cuh"
+#include "tma.cuh"
+
+#include <type_traits>
 
 namespace gconv {
 
@@ -37,13 +43,15 @@ namespace gconv {
 // weight pairs fit in about 100 registers.
 template <typename T>
 constexpr int row8_vec(int K) {
-    return K <= 3 ? (sizeof(T) == 4 ? 4 : 8) : 2;
+    return K <= 3 ? 4 : 2;
 }
 // Output pixels per thread and the CTA size cap, which sets how many
 // registers a thread may use (weights + R*S accumulator pairs + window).
 constexpr int row8_s(int K) { return K == 5 ? 4 : 2; }
-constexpr int row8_max_threads(int K) { return K <= 3 ? 256 : (K <= 5 ? 448 : 336); }
-constexpr int kRow8Stages = 6;          // ring depth: 5 input rows in flight
+constexpr int row8_max_threads(int K) { return K <= 3 ? 512 : (K <= 5 ? 384 : 336); }
+constexpr int kRow8MaxStages = 8;
+// Input rows per stage: one rotation period of the accumulator sets.
+constexpr int row8_rows_per_stage(int K, int SH) { return SH * ((K + SH - 1) / SH); }
 
 // Host-computed geometry of one launch.
 struct Row8Geom {
@@ -51,25 +59,15 @@ struct Row8Geom {
     int PG;         // pixel groups per column chunk (threads along columns)
     int OWc;        // output columns per chunk = PG * S
     int CC, HC;     // column chunks, channel chunks
-    int Win;        // input pixels per staged row segment
-    int pitch;      // bytes per staged pixel (multiple of 16)
-    int stage;      // bytes per stage
-    int chunk16;    // 16-byte copies per staged pixel
+    int Win;        // input pixels per staged row segment (TMA box width)
+    int pitch;      // bytes per staged pixel = chunk channels * element size
+    int box_bytes;  // bytes one row copy delivers
+    int stage;      // bytes per stage (box_bytes rounded up to 128)
+    int NS;         // stages in the ring
     int units;      // output rows in the flat list
     int ctas;
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-// A run: output rows [oh0, oh0 + rows) of one (n, cc, hc).
 struct Row8Run {
     int n, cc, hc, oh0, rows, nin;   // nin = input rows the run reads
 };
@@ -95,25 +93,45 @@ __device__ __forceinline__ Row8Run row8_run_at(int u, int o1, int OH, int CC, in
 constexpr int fdiv(int a, int b) { return (a >= 0) ? a / b : -((-a + b - 1) / b); }
 constexpr int fmod_pos(int a, int b) { return ((a % b) + b) % b; }
 
+// Shared-memory vector loads through 32-bit shared addresses.
+template <int BYTES> struct Lds;
+template <> struct Lds<4> {
+    template <typename V> static __device__ __forceinline__ void load(V &v, uint32_t a) {
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v.w[0]) : "r"(a));
+    }
+};
+template <> struct Lds<8> {
+    template <typename V> static __device__ __forceinline__ void load(V &v, uint32_t a) {
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.w[0]), "=r"(v.w[1]) : "r"(a));
+    }
+};
+template <> struct Lds<16> {
+    template <typename V> static __device__ __forceinline__ void load(V &v, uint32_t a) {
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "r"(a));
+    }
+};
+
 template <typename T, int K, int SH>
 __global__ void __launch_bounds__(row8_max_threads(K), 1)
-row8_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
-            T *__restrict__ y, Params p, Row8Geom g) {
+row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
+            const T *__restrict__ w, const T *__restrict__ b, T *__restrict__ y, Params p,
+            Row8Geom g) {
     constexpr int SW = SH;                       // square strides only
     constexpr int VEC = row8_vec<T>(K);
     constexpr int P = VEC / 2;                   // channel pairs per thread
     constexpr int S = row8_s(K);
     constexpr int VB = VEC * (int)sizeof(T);     // bytes per vector
     constexpr int R = (K + SH - 1) / SH;         // output rows open at once
-    constexpr int U = SH * R;                    // rotation period of the sets
+    constexpr int U = SH * R;                    // rotation period = input rows per stage
     constexpr int WIN = (S - 1) * SW + K;        // input vectors per window
-    constexpr int NS = kRow8Stages;
     using V = Vec<T, VEC>;
     using IO = VecIO<VB>;
-    extern __shared__ __align__(16) unsigned char row8_ring[];
+    extern __shared__ __align__(128) unsigned char row8_ring[];
+    (void)x;
 
     const int t = threadIdx.x;
-    const int nthreads = g.CVc * g.PG;
     const int cvl = t % g.CVc;
     const int pg = t / g.CVc;
 
@@ -123,69 +141,86 @@ row8_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
     const int o1 = o0 + per + ((int)blockIdx.x < extra ? 1 : 0);
     if (o0 >= o1) return;
 
-    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(row8_ring);
-    const int c_bytes = p.C_out * (int)sizeof(T);
+    const uint32_t ring = smem_addr(row8_ring);
+    const uint32_t bars = ring + (uint32_t)(g.NS * g.stage);   // NS mbarriers
+    volatile int *failed = reinterpret_cast<volatile int *>(row8_ring + g.NS * g.stage + 8 * g.NS);
+    // fp32 weights [tap][chunk channel] and bias, after the barriers
+    float *wsm = reinterpret_cast<float *>(row8_ring + g.NS * g.stage + 8 * g.NS + 16);
+    const int row_bytes = g.Win * g.pitch;       // one staged input row
 
-    const int64_t xs3b = p.xs[3] * (int64_t)sizeof(T);
-    // This thread's first 16-byte copy of a stage and the step between its
-    // copies (copy q = t + i * nthreads covers pixel q / chunk16).
-    const int cp_pix0 = t / g.chunk16, cp_sub0 = t - cp_pix0 * g.chunk16;
-    const int cp_dpix = nthreads / g.chunk16, cp_dsub = nthreads - cp_dpix * g.chunk16;
-
-    // Producer state: the run and input row of the next entry to issue.
-    Row8Run prun = row8_run_at<K, SH>(o0, o1, p.OH, g.CC, g.HC);
-    int pnext_u = o0 + prun.rows;
-    int pr = 0;
+    // Producer (thread 0 only): the run and stage of the next box.  A stage
+    // holds U consecutive input rows of one run.
+    Row8Run prun;
+    int pnext_u = 0, pst = 0, pnst = 0, pslot = 0;
     bool pdone = false;
-    int pslot = 0;
-
-    // Copy the producer's next input row into its stage (nothing once the
-    // list is exhausted) and commit one group, so group counts stay uniform.
     auto issue = [&]() {
-        if (!pdone) {
-            const int ih = prun.oh0 * SH - p.pbh + pr;
-            const bool row_ok = ih >= 0 && ih < p.H;
-            const int iw_start = prun.cc * g.OWc * SW - p.pbw;
-            const int cb0 = prun.hc * g.CVc * VB;
-            const uint32_t dst0 = ring + (uint32_t)(pslot * g.stage);
-            const char *src_row =
-                reinterpret_cast<const char *>(x + (int64_t)prun.n * p.xs[0] +
-                                               (int64_t)(row_ok ? ih : 0) * p.xs[2]) + cb0;
-            int pix = cp_pix0, sub = cp_sub0;
-            while (pix < g.Win) {
-                const int iw = iw_start + pix;
-                const int cbyte = sub * 16;
-                int bytes = c_bytes - (cb0 + cbyte);
-                bytes = bytes > 16 ? 16 : bytes;
-                const bool ok = row_ok && iw >= 0 && iw < p.W && bytes > 0;
-                const char *src = ok ? src_row + (int64_t)iw * xs3b + cbyte
-                                     : reinterpret_cast<const char *>(x);
-                cp_async16(dst0 + (uint32_t)(pix * g.pitch + cbyte), src, ok ? bytes : 0);
-                pix += cp_dpix;
-                sub += cp_dsub;
-                if (sub >= g.chunk16) { sub -= g.chunk16; ++pix; }
-            }
-            if (++pr == prun.nin) {
-                if (pnext_u >= o1) {
-                    pdone = true;
-                } else {
-                    prun = row8_run_at<K, SH>(pnext_u, o1, p.OH, g.CC, g.HC);
-                    pnext_u += prun.rows;
-                    pr = 0;
-                }
+        if (pdone) return;
+        const uint32_t bar = bars + 8u * pslot;
+        mbar_arrive_expect_tx(bar, (uint32_t)g.box_bytes);
+        tma_load_4d(ring + (uint32_t)(pslot * g.stage), &xmap, bar, prun.hc * g.CVc * VEC,
+                    prun.cc * g.OWc * SW - p.pbw, prun.oh0 * SH - p.pbh + pst * U, prun.n);
+        if (++pslot == g.NS) pslot = 0;
+        if (++pst == pnst) {
+            if (pnext_u >= o1) {
+                pdone = true;
+            } else {
+                prun = row8_run_at<K, SH>(pnext_u, o1, p.OH, g.CC, g.HC);
+                pnext_u += prun.rows;
+                pst = 0;
+                pnst = (prun.nin + U - 1) / U;
             }
         }
-        cp_async_commit();
-        if (++pslot == NS) pslot = 0;
     };
-
-#pragma unroll 1
-    for (int i = 0; i < NS - 1; ++i) issue();   // prologue: NS - 1 rows in flight
-
     float2 wr[K][K][P];
     float2 bias[P];
-    int loaded_hc = -1;
-    int cslot = 0;                  // stage of the consumer's next input row
+    // Stage chunk hc's weights and bias through shared memory with coalesced
+    // loads ([tap][channel] fp32), then take this thread's channel pairs.
+    auto stage_weights = [&](int hc) {
+        const int cb = g.CVc * VEC, cfirst = hc * cb;
+        for (int e = t; e < cb * K * K; e += blockDim.x) {
+            const int cl = e / (K * K), tap = e - cl * (K * K);
+            const int c = cfirst + cl;
+            const int kh = tap / K, kw = tap - kh * K;
+            wsm[tap * cb + cl] =
+                c < p.C_out ? load_f32(w + (int64_t)c * p.ws[0] + kh * p.ws[2] + kw * p.ws[3]) : 0.f;
+        }
+        for (int cl = t; cl < cb; cl += blockDim.x) {
+            const int c = cfirst + cl;
+            wsm[K * K * cb + cl] = (c < p.C_out && p.has_bias) ? load_f32(b + (int64_t)c * p.bs) : 0.f;
+        }
+    };
+    auto take_weights = [&]() {
+        const int cb = g.CVc * VEC;
+        const float2 *src = reinterpret_cast<const float2 *>(wsm) + cvl * P;
+#pragma unroll
+        for (int kh = 0; kh < K; ++kh)
+#pragma unroll
+            for (int kw = 0; kw < K; ++kw)
+#pragma unroll
+                for (int k = 0; k < P; ++k) wr[kh][kw][k] = src[((kh * K + kw) * cb) / 2 + k];
+#pragma unroll
+        for (int k = 0; k < P; ++k) bias[k] = src[(K * K * cb) / 2 + k];
+    };
+    // The first run's weights are fetched before the row stream starts:
+    // issued behind it they would wait for it.
+    int loaded_hc = row8_run_at<K, SH>(o0, o1, p.OH, g.CC, g.HC).hc;
+    stage_weights(loaded_hc);
+
+    if (t == 0) {
+        tma_prefetch_map(&xmap);
+        for (int i = 0; i < g.NS; ++i) mbar_init(bars + 8u * i, 1);
+        *failed = 0;
+        fence_barrier_init();
+        prun = row8_run_at<K, SH>(o0, o1, p.OH, g.CC, g.HC);
+        pnext_u = o0 + prun.rows;
+        pnst = (prun.nin + U - 1) / U;
+        for (int i = 0; i < g.NS; ++i) issue();   // prologue: NS stages in flight
+    }
+    __syncthreads();
+    take_weights();
+
+    int cslot = 0;        // stage of the consumer's next box
+    uint32_t cphase = 0;  // parity of that stage's current use
 
     int u = o0;
     while (u < o1) {
@@ -195,23 +230,10 @@ row8_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
         const bool active = c0 < p.C_out;
         if (run.hc != loaded_hc) {
             loaded_hc = run.hc;
-#pragma unroll
-            for (int kh = 0; kh < K; ++kh)
-#pragma unroll
-                for (int kw = 0; kw < K; ++kw)
-#pragma unroll
-                    for (int k = 0; k < P; ++k) {
-                        const T *wp = w + (int64_t)(c0 + 2 * k) * p.ws[0] + kh * p.ws[2] +
-                                      kw * p.ws[3];
-                        wr[kh][kw][k] = active ? make_float2(load_f32(wp), load_f32(wp + p.ws[0]))
-                                               : make_float2(0.f, 0.f);
-                    }
-#pragma unroll
-            for (int k = 0; k < P; ++k)
-                bias[k] = (active && p.has_bias)
-                              ? make_float2(load_f32(b + (int64_t)(c0 + 2 * k) * p.bs),
-                                            load_f32(b + (int64_t)(c0 + 2 * k + 1) * p.bs))
-                              : make_float2(0.f, 0.f);
+            __syncthreads();
+            stage_weights(loaded_hc);
+            __syncthreads();
+            take_weights();
         }
         // Accumulator set s serves the output rows j with j mod R == s; it
         // is reset to the bias right after its row's last input row.
@@ -224,71 +246,81 @@ row8_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
                 for (int k = 0; k < P; ++k) acc[s][i][k] = bias[k];
 
         const int ow0 = run.cc * g.OWc + pg * S;
-        T *ybase = y + (int64_t)run.n * p.ys[0] + (int64_t)ow0 * p.ys[3] + c0;
-        const unsigned char *win0 = row8_ring + cvl * VB + pg * S * SW * g.pitch;
+        // the run's first output row at this thread's pixels and channels
+        T *ynext = y + (int64_t)run.n * p.ys[0] + (int64_t)run.oh0 * p.ys[2] +
+                   (int64_t)ow0 * p.ys[3] + (active ? c0 : 0);
+        const uint32_t win0 = ring + (uint32_t)(cvl * VB + pg * S * SW * g.pitch);
 
         for (int r0 = 0; r0 < run.nin; r0 += U) {
+            if (!mbar_wait(bars + 8u * cslot, cphase)) *failed = 1;
+            const uint32_t stage0 = win0 + (uint32_t)(cslot * g.stage);
+            // Straight-line over the stage's U rows (no branches around the
+            // arithmetic, so the scheduler can overlap the rows' loads):
+            // every row is multiplied into every set it feeds; sets whose
+            // output row lies outside the run collect values that are never
+            // stored, and each set is reset right after its last tap row.
 #pragma unroll
             for (int ph = 0; ph < U; ++ph) {
                 const int r = r0 + ph;
-                if (r < run.nin) {
-                    // Input row r: complete for this thread, then for all; the
-                    // stage read one row ago is free and is refilled at once.
-                    cp_async_wait<NS - 2>();
-                    __syncthreads();
-                    issue();
-                    if (active) {
-                        const unsigned char *st = win0 + cslot * g.stage;
-                        float2 xr[WIN][P];
+                const uint32_t st = stage0 + (uint32_t)(ph * row_bytes);
+                float2 xr[WIN][P];
 #pragma unroll
-                        for (int j = 0; j < WIN; ++j) {
-                            V v;
-                            IO::load_shared(v, st + j * g.pitch);
-                            widen<T, VEC>(v, xr[j]);
-                        }
+                for (int j = 0; j < WIN; ++j) {
+                    V v;
+                    Lds<VB>::load(v, st + (uint32_t)(j * g.pitch));
+                    widen<T, VEC>(v, xr[j]);
+                }
 #pragma unroll
-                        for (int kh = 0; kh < K; ++kh) {
-                            const int d = ph - kh;               // (r - kh) - r0
-                            if (fmod_pos(d, SH) != 0) continue;  // no output row has tap row kh here
-                            const int set = fmod_pos(fdiv(d, SH), R);
-                            const int jn = r - kh;   // SH * (output row within the run)
-                            if (jn >= 0 && jn < run.rows * SH) {
+                for (int kh = 0; kh < K; ++kh) {
+                    const int d = ph - kh;               // (r - kh) - r0
+                    if (fmod_pos(d, SH) != 0) continue;  // no output row has tap row kh here
+                    const int set = fmod_pos(fdiv(d, SH), R);
 #pragma unroll
-                                for (int i = 0; i < S; ++i)
+                    for (int i = 0; i < S; ++i)
 #pragma unroll
-                                    for (int kw = 0; kw < K; ++kw)
+                        for (int kw = 0; kw < K; ++kw)
 #pragma unroll
-                                        for (int k = 0; k < P; ++k)
-                                            fma2(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw][k]);
-                            }
-                        }
-                        // The output row whose last tap row this was is done.
-                        {
-                            const int d = ph - (K - 1);
-                            if (fmod_pos(d, SH) == 0) {
-                                const int set = fmod_pos(fdiv(d, SH), R);
-                                const int jn = r - (K - 1);
-                                if (jn >= 0) {
-                                    T *yrow = ybase + (int64_t)(run.oh0 + jn / SH) * p.ys[2];
+                            for (int k = 0; k < P; ++k)
+                                if constexpr (K >= 5)   // measured: packed wins for 5x5/7x7, scalar for 3x3
+                                    fma2_packed(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw][k]);
+                                else
+                                    fma2(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw][k]);
+                }
+                // The output row whose last tap row this was is done.
+                const int d = ph - (K - 1);
+                if (fmod_pos(d, SH) == 0) {
+                    const int set = fmod_pos(fdiv(d, SH), R);
+                    const int jn = r - (K - 1);          // SH * output row within the run
+                    if (active && jn >= 0 && jn < run.rows * SH) {
+                        const bool bad = *failed != 0;
+                        T *yrow = ynext + (int64_t)(jn / SH) * p.ys[2];
 #pragma unroll
-                                    for (int i = 0; i < S; ++i)
-                                        if (ow0 + i < p.OW)
-                                            IO::store(yrow + (int64_t)i * p.ys[3],
-                                                      pack_pairs<T, VEC>(acc[set][i]));
-                                }
+                        for (int i = 0; i < S; ++i) {
+                            if (ow0 + i < p.OW) {
+                                float2 o[P];
 #pragma unroll
-                                for (int i = 0; i < S; ++i)
-#pragma unroll
-                                    for (int k = 0; k < P; ++k) acc[set][i][k] = bias[k];
+                                for (int k = 0; k < P; ++k)
+                                    o[k] = bad ? make_float2(__int_as_float(0x7fc00000),
+                                                             __int_as_float(0x7fc00000))
+                                               : acc[set][i][k];
+                                IO::store(yrow + (int64_t)i * p.ys[3], pack_pairs<T, VEC>(o));
                             }
                         }
                     }
-                    if (++cslot == NS) cslot = 0;
+#pragma unroll
+                    for (int i = 0; i < S; ++i)
+#pragma unroll
+                        for (int k = 0; k < P; ++k) acc[set][i][k] = bias[k];
                 }
             }
+            if (++cslot == g.NS) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
+            __syncthreads();          // every thread is done with that stage
+            if (t == 0) issue();      // refill it with the box NS stages ahead
         }
     }
-    cp_async_wait<0>();
 }
 
 // Launch geometry for one call; false when the shape does not fit.
@@ -300,23 +332,30 @@ bool row8_geometry(const Params &p, Row8Geom &g) {
     constexpr int MAXT = row8_max_threads(K);
     if (p.C_out % VEC != 0) return false;
     const int CV = p.C_out / VEC;
-    g.CVc = CV < MAXT ? CV : MAXT;
+    int cv_cap = MAXT < 256 / VEC ? MAXT : 256 / VEC;   // TMA box: <= 256 channels
+    g.CVc = CV < cv_cap ? CV : cv_cap;
+    if ((g.CVc * VB) % 16 != 0) return false;            // box rows of whole 16-byte units
     g.HC = (CV + g.CVc - 1) / g.CVc;
     const int pg_max = MAXT / g.CVc;
     const int pg_need = (p.OW + S - 1) / S;
-    // Split the columns evenly over the fewest chunks that fit the CTA.
-    const int cc = (pg_need + pg_max - 1) / pg_max;
+    // Split the columns evenly over the fewest chunks that fit the CTA and
+    // keep each staged segment within the 256-pixel TMA box.
+    int cc = (pg_need + pg_max - 1) / pg_max;
+    for (;; ++cc) {
+        const int pg = (pg_need + cc - 1) / cc;
+        if ((pg * S - 1) * p.sw + K <= 256) break;
+    }
     g.PG = (pg_need + cc - 1) / cc;
     g.OWc = g.PG * S;
     g.CC = (p.OW + g.OWc - 1) / g.OWc;
     g.Win = (g.OWc - 1) * p.sw + K;
-    g.chunk16 = (g.CVc * VB + 15) / 16;
-    g.pitch = g.chunk16 * 16;
-    g.stage = g.Win * g.pitch;
-    if ((size_t)g.stage * kRow8Stages > 220 * 1024) return false;
-    // byte offsets within one image row fit in 32 bits
-    if ((int64_t)p.W * p.xs[3] * (int64_t)sizeof(T) + p.C_out * (int64_t)sizeof(T) > INT32_MAX)
-        return false;
+    g.pitch = g.CVc * VB;
+    g.box_bytes = g.Win * g.pitch * row8_rows_per_stage(K, p.sh);
+    g.stage = (g.box_bytes + 127) / 128 * 128;
+    int ns = (200 * 1024 - (K * K + 1) * g.CVc * VEC * 4) / g.stage;
+    if (ns > kRow8MaxStages) ns = kRow8MaxStages;
+    if (ns < 2) return false;
+    g.NS = ns;
     const int64_t units = (int64_t)p.N * g.CC * g.HC * p.OH;
     if (units > INT32_MAX / 2) return false;
     g.units = (int)units;
@@ -324,17 +363,34 @@ bool row8_geometry(const Params &p, Row8Geom &g) {
     return true;
 }
 
+template <typename T> constexpr CUtensorMapDataType tma_dtype() {
+    return sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                          : (std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
 template <typename T, int K, int SH>
 cudaError_t row8_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
+    constexpr int VEC = row8_vec<T>(K);
     Row8Geom g;
     if (!row8_geometry<T, K>(p, g)) return cudaErrorNotSupported;
-    const size_t smem = (size_t)kRow8Stages * g.stage;
+    // x as (C, W, H, N), innermost first; a box is one row segment.
+    const uint64_t es = sizeof(T);
+    const uint64_t dims[4] = {(uint64_t)p.C_out, (uint64_t)p.W, (uint64_t)p.H, (uint64_t)p.N};
+    const uint64_t strides[3] = {(uint64_t)p.xs[3] * es, (uint64_t)p.xs[2] * es,
+                                 (uint64_t)p.xs[0] * es};
+    const uint32_t box[4] = {(uint32_t)(g.CVc * VEC), (uint32_t)g.Win,
+                             (uint32_t)row8_rows_per_stage(K, SH), 1u};
+    CUtensorMap map;
+    if (!tma_encode_4d(&map, tma_dtype<T>(), q.x, dims, strides, box)) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)g.NS * g.stage + 8 * (size_t)g.NS + 16 +
+                        (size_t)(K * K + 1) * g.CVc * VEC * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(row8_kernel<T, K, SH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     row8_kernel<T, K, SH><<<g.ctas, g.CVc * g.PG, smem, s>>>(
-        static_cast<const T *>(q.x), static_cast<const T *>(q.w), static_cast<const T *>(q.b),
-        static_cast<T *>(q.y), p, g);
+        map, static_cast<const T *>(q.x), static_cast<const T *>(q.w),
+        static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
     return cudaGetLastError();
 }
 

@@ -3,11 +3,11 @@
 //
 // fp32 accumulation throughout.  16-bit inputs are widened once per load
 // (bf16 -> fp32 is a 16-bit shift, fp16 -> fp32 the hardware conversion),
-// then every product is a scalar fp32 FMA.  Values travel as channel pairs
+// then every product is an fp32 FMA.  Values travel as channel pairs
 // (float2) because two 16-bit channels share one 32-bit word.  Measured on
 // GB300: the packed fma.rn.f32x2 issues as one instruction but runs only on
-// one of the two FMA pipes, so at the occupancy these kernels run at, scalar
-// FMAs (which use both pipes) finish the same work 1.7x sooner.
+// one of the two FMA pipes, while scalar FMAs use both; which is faster
+// depends on the kernel (issue slots vs latency), so both forms exist.
 #pragma once
 
 #include "device_common.cuh"
@@ -85,6 +85,11 @@ __device__ __forceinline__ void zero(float2 (&f)[VEC / 2]) {
 __device__ __forceinline__ void fma2(float2 &acc, float2 w, float2 x) {
     acc.x = fmaf(w.x, x.x, acc.x);
     acc.y = fmaf(w.y, x.y, acc.y);
+}
+
+// The same with one packed fma.rn.f32x2 (both lanes round to nearest).
+__device__ __forceinline__ void fma2_packed(float2 &acc, float2 w, float2 x) {
+    acc = __ffma2_rn(w, x, acc);
 }
 
 // Round VEC fp32 values (as pairs) to T and pack them.
