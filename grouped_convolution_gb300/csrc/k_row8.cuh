@@ -177,12 +177,24 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     // loads ([tap][channel] fp32), then take this thread's channel pairs.
     auto stage_weights = [&](int hc) {
         const int cb = g.CVc * VEC, cfirst = hc * cb;
-        for (int e = t; e < cb * K * K; e += blockDim.x) {
-            const int cl = e / (K * K), tap = e - cl * (K * K);
-            const int c = cfirst + cl;
-            const int kh = tap / K, kw = tap - kh * K;
-            wsm[tap * cb + cl] =
-                c < p.C_out ? load_f32(w + (int64_t)c * p.ws[0] + kh * p.ws[2] + kw * p.ws[3]) : 0.f;
+        constexpr int QW = 8;   // loads in flight per thread before their stores
+        for (int e0 = t; e0 < cb * K * K; e0 += QW * blockDim.x) {
+            float v[QW];
+#pragma unroll
+            for (int q = 0; q < QW; ++q) {
+                const int e = e0 + q * blockDim.x;
+                const int cl = e / (K * K), tap = e - cl * (K * K);
+                const int c = cfirst + cl;
+                const int kh = tap / K, kw = tap - kh * K;
+                v[q] = (e < cb * K * K && c < p.C_out)
+                           ? load_f32(w + (int64_t)c * p.ws[0] + kh * p.ws[2] + kw * p.ws[3]) : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < QW; ++q) {
+                const int e = e0 + q * blockDim.x;
+                const int cl = e / (K * K), tap = e - cl * (K * K);
+                if (e < cb * K * K) wsm[tap * cb + cl] = v[q];
+            }
         }
         for (int cl = t; cl < cb; cl += blockDim.x) {
             const int c = cfirst + cl;
