@@ -123,6 +123,37 @@ def test_picker_and_bias_flag(schedule, bias):
     check(wl, x, w, b, y)
 
 
+# dw_mult band geometry: several row bands, several column chunks, every
+# window offset against the 16-byte grid (left padding 0..3), row and column
+# stride 2 with the band shrunk to fit, multipliers with and without
+# 4-channel blocking, rows with and without 16-byte alignment.
+MULT_CASES = [
+    # name, N, m, C, H, W, KH, KW, stride, pad_before, pad_after
+    ("tall_pb0", 1, 4, 3, 300, 30, 3, 3, (1, 1), (1, 0), (1, 3)),
+    ("tall_pb1", 1, 4, 3, 290, 40, 4, 4, (1, 1), (1, 1), (2, 2)),
+    ("pb2_m3", 2, 3, 2, 61, 48, 5, 5, (1, 1), (2, 2), (2, 2)),
+    ("pb3_m8", 1, 8, 2, 40, 53, 7, 7, (1, 1), (3, 3), (3, 3)),
+    ("wide_m2", 1, 2, 2, 9, 2100, 3, 9, (1, 1), (1, 4), (1, 4)),
+    ("wide_s2", 1, 4, 2, 33, 1504, 3, 3, (2, 2), (1, 1), (1, 1)),
+    ("s2_k9_m16", 1, 16, 1, 45, 80, 9, 9, (2, 2), (4, 4), (4, 4)),
+    ("s3_1x1", 1, 5, 2, 20, 41, 1, 1, (3, 1), (0, 0), (0, 0)),
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("case", MULT_CASES, ids=[c[0] for c in MULT_CASES])
+def test_dw_mult_geometry_matches_oracle(case, dtype):
+    name, N, m, C, H, W, KH, KW, s, pb, pa = case
+    wl = ConvWorkload(name, 31 + MULT_CASES.index(case), N=N, C_in=C, H=H, W=W, C_out=C * m,
+                      groups=C, KH=KH, KW=KW, stride=s, pad_before=pb, pad_after=pa,
+                      dtype=dtype, channels_last=False, bias=m % 2 == 0)
+    x, w, b = make_inputs(wl)
+    y = run_gpu(wl, x, w, b, "dw_mult")
+    assert y is not None, "dw_mult must take this case"
+    RAN["dw_mult"] += 1
+    check(wl, x, w, b, y)
+
+
 # ------------------------------------------------------------ bit-exact
 
 @pytest.mark.parametrize("schedule", SCHED)
