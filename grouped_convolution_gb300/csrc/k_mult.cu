@@ -10,17 +10,15 @@ bool mult_supports(const gconv_desc &d, const Ptrs &q) {
     if (d.layout != GCONV_LAYOUT_NCHW) return false;
     if (d.KW > kMultMaxKW) return false;
     if (d.stride[1] != 1 && d.stride[1] != 2) return false;
-    // x must have unit stride along W (NCHW order guarantees it); rows that
-    // are not 16-byte aligned are loaded element by element.
+    // x must have unit stride along W (NCHW order guarantees it); x that a
+    // tensor map cannot describe is staged with plain loads.
     if (d.x_strides[3] != 1) return false;
     const int es = dtype_size(d.dtype);
     (void)q;
     Params p = make_params(d);
     MultGeom g;
     if (!mult_geometry(p, es, g)) return false;
-    // the band offsets are packed in 16 bits
-    if (g.rows_in >= (1 << 15) || g.cpr >= (1 << 16)) return false;
-    return mult_smem_bytes(p, g) <= 200 * 1024;
+    return true;
 }
 
 cudaError_t mult_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *launches) {

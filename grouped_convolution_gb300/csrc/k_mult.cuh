@@ -9,35 +9,39 @@
 //    column chunk), column chunk fastest and c slowest, so a persistent CTA
 //    restages the m*KH*KW weights only when c changes.  Items are split
 //    evenly over two CTAs per SM and stepped without divisions.
-//  - The band's input rows ((BR-1)*SH + KH rows) are fetched one item ahead
-//    as 16-byte chunks aligned in global memory (zeros outside the image)
-//    into registers, then widened once to fp32 into shared memory with
-//    16-byte stores.  Shared column 0 is the first window column rounded
-//    down to a multiple of 4, so chunks land on 16-byte shared boundaries;
-//    every thread's window then starts MIS (0..3, the same for every thread
-//    and item) columns past a 16-byte boundary, and MIS is a template
-//    parameter of the tap loop, so the window is read with 16-byte loads and
-//    the taps index registers at compile-time offsets.
+//  - An item's input band ((BR-1)*SH + KH rows) arrives as one TMA tensor
+//    box, two items ahead, in a two-stage ring of raw (input dtype) boxes
+//    with bounded mbarrier waits; the box starts at the window's first
+//    column rounded down to 16 bytes (a TMA rule) and the tensor map's zero
+//    fill supplies the padding.  When x cannot be described by a tensor map
+//    (unaligned base or strides) all threads fill the box with plain loads.
+//  - A widening pass copies the box into a double-buffered fp32 band,
+//    dropping the SHIFT columns before the first window column, so every
+//    thread's window starts on a 16-byte shared boundary.  One barrier per
+//    item separates the widening pass from the arithmetic.
 //  - Thread (row pair, pixel group) computes S consecutive output pixels of
 //    RT = 2 consecutive output rows for MB output channels at a time: each
-//    staged input row is loaded once and multiplied into both output rows
-//    it feeds; per tap one broadcast shared load of MB weights feeds MB*S
-//    FMAs per output row.
+//    band row is loaded once and multiplied into both output rows it feeds;
+//    with MB = 4 the products run as packed fp32x2 FMAs over channel pairs.
+//    The tap loop is unrolled for kernel widths 3, 4, 5, 7 and predicated
+//    for the others.
 //  - fp32 accumulation from the bias, one rounding, 16-byte stores of S
 //    pixels where the row allows it.
 #pragma once
 
 #include "device_common.cuh"
 #include "gconv_internal.h"
+#include "tma.cuh"
 
 namespace gconv {
 
 constexpr int kMultThreads = 256;
 constexpr int kMultRT = 2;           // output rows per thread
-constexpr int kMultMaxChunks = 4;    // 16-byte global chunks per thread per band
 constexpr int kMultMaxKW = 9;
 constexpr int kMultCtasPerSM = 2;
 constexpr int kMultSMs = 152;
+constexpr int kMultSmemCap = 110 * 1024;   // two CTAs per SM
+constexpr int kMultBoxMax = 256;           // TMA box extent limit
 
 struct MultGeom {
     int m;          // multiplier (Cout_g)
@@ -48,29 +52,30 @@ struct MultGeom {
     int OWc, CC;    // output columns per chunk, column chunks
     int bands;
     int rows_in;    // input rows per band
-    int mis;        // first window column minus shared column 0 (0..3)
-    int coff;       // shared column 0 minus the first chunk's column (0 or 4)
-    int cpr;        // 16-byte global chunks per band row
-    int nchunks;    // chunks per band
-    int pitch;      // fp32 elements per shared row (multiple of 4)
+    int shift;      // first window column minus the box's first column
+    int spr;        // 4-column slots per band row
+    int BWX;        // box width (elements, multiple of 16 bytes)
+    int pitch;      // fp32 elements per band row (multiple of 4)
+    int stage;      // bytes per raw stage (multiple of 128)
+    int band_off;   // byte offsets in shared memory
+    int w_off;
+    int bar_off;
+    int smem;       // bytes of shared memory
+    int box_bytes;  // bytes one box delivers
     int items;
     int ctas;
-    int vec_load;   // rows of x allow 16-byte chunk loads
+    int use_tma;    // x is described by a tensor map
     int vec_store;  // rows of y allow 16-byte stores of S pixels
 };
 
-// 16-byte shared loads a thread's window needs at most.
-template <int S, int SW, int MIS>
-constexpr int mult_wl4() { return (MIS + (S - 1) * SW + kMultMaxKW + 3) / 4; }
+// 16-byte shared loads of a thread's window (KW = 0: any width up to 9).
+template <int S, int SW, int KW>
+constexpr int mult_wl4() { return ((S - 1) * SW + (KW ? KW : kMultMaxKW) + 3) / 4; }
 
-inline int mult_floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
-
-// Geometry for element size es; false when the band does not fit the
-// per-thread chunk budget or the item count overflows.
 // Band geometry for CC column chunks and at most tr_cap thread rows; false
-// when the band's chunks exceed the per-thread budget.
+// when the box or shared memory does not fit.
 inline bool mult_band(const Params &p, int es, int CC, int tr_cap, MultGeom &g) {
-    const int CE = 16 / es;                 // elements per 16-byte chunk
+    const int CE = 16 / es;                 // elements per 16 bytes
     const int pg_need = (p.OW + g.S - 1) / g.S;
     g.CC = CC;
     g.PGn = (pg_need + CC - 1) / CC;
@@ -86,31 +91,33 @@ inline bool mult_band(const Params &p, int es, int CC, int tr_cap, MultGeom &g) 
     g.BR = g.TR * kMultRT;
     g.bands = (p.OH + g.BR - 1) / g.BR;
     g.rows_in = (g.BR - 1) * p.sh + p.KH;
-    // Window of column chunk cc starts at iw0 = cc*OWc*sw - pbw; OWc*sw is a
-    // multiple of CE (and of 4), so mis and coff do not depend on cc.
-    const int iw0 = -p.pbw;
-    const int origin = mult_floor_div(iw0, 4) * 4;
-    g.mis = iw0 - origin;
-    const int cbase = mult_floor_div(origin, CE) * CE;
-    g.coff = origin - cbase;
-    const int need = g.mis + (g.OWc - 1) * p.sw + p.KW;   // shared columns used
-    g.cpr = (g.coff + need + CE - 1) / CE;
-    g.nchunks = g.rows_in * g.cpr;
-    if (g.nchunks > kMultThreads * kMultMaxChunks) return false;
-    // Every thread's 16-byte window loads stay inside the row.
-    const int wl4 = (3 + (g.S - 1) * p.sw + kMultMaxKW + 3) / 4;
+    if (g.rows_in > kMultBoxMax) return false;
+    // Chunk cc's first window column is cc*OWc*sw - pbw; OWc*sw is a
+    // multiple of CE, so its offset from the 16-byte grid does not depend on cc.
+    g.shift = ((-p.pbw) % CE + CE) % CE;
+    const int need = (g.OWc - 1) * p.sw + p.KW;   // band columns the outputs use
+    g.spr = (need + 3) / 4;
+    g.BWX = (g.shift + 4 * g.spr + CE - 1) / CE * CE;
+    if (g.BWX > kMultBoxMax) return false;
+    // Every thread's 16-byte window loads stay inside its band row.
+    const int wl4 = ((g.S - 1) * p.sw + kMultMaxKW + 3) / 4;
     const int span = (g.PGn - 1) * g.S * p.sw + 4 * wl4;
-    g.pitch = ((need > span ? need : span) + 3) / 4 * 4;
-    return true;
+    g.pitch = 4 * g.spr > span ? 4 * g.spr : (span + 3) / 4 * 4;
+    g.box_bytes = g.rows_in * g.BWX * es;
+    g.stage = (g.box_bytes + 127) / 128 * 128;
+    g.band_off = 2 * g.stage;
+    g.w_off = g.band_off + 2 * g.rows_in * g.pitch * 4;
+    g.bar_off = g.w_off + ((p.KH * p.KW * g.m + g.m) * 4 + 15) / 16 * 16;
+    g.smem = g.bar_off + 32;   // two mbarriers, failure flag
+    return g.smem <= kMultSmemCap;
 }
 
 // Geometry for element size es: the fewest column chunks, then the most
-// thread rows, whose band fits the chunk budget.  False when none does or
-// the item count overflows.
+// thread rows, that fit.  False when none does or the item count overflows.
 inline bool mult_geometry(const Params &p, int es, MultGeom &g) {
     g.m = p.Cout_g;
     g.S = 16 / es;
-    g.vec_load = 0;
+    g.use_tma = 0;
     g.vec_store = 0;
     const int pg_need = (p.OW + g.S - 1) / g.S;
     bool ok = false;
@@ -121,15 +128,11 @@ inline bool mult_geometry(const Params &p, int es, MultGeom &g) {
     }
     if (!ok) return false;
     const int64_t items = (int64_t)p.C_in * p.N * g.bands * g.CC;
-    if (items > INT32_MAX) return false;
+    if (items > INT32_MAX - 2) return false;
     g.items = (int)items;
     const int cap = kMultSMs * kMultCtasPerSM;
     g.ctas = g.items < cap ? g.items : cap;
     return true;
-}
-
-inline size_t mult_smem_bytes(const Params &p, const MultGeom &g) {
-    return ((size_t)g.rows_in * g.pitch + (size_t)p.KH * p.KW * g.m + g.m) * sizeof(float);
 }
 
 // Division-free cursor over items (cc fastest, then band, image, channel).
@@ -154,37 +157,131 @@ struct MultItem {
     }
 };
 
-// Widen a 16-byte chunk of T into CE fp32 values.
-template <typename T>
-__device__ __forceinline__ void mult_widen(const uint4 &v, float (&f)[16 / sizeof(T)]) {
-    if constexpr (sizeof(T) == 4) {
-        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
-    } else {
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+// Round S fp32 values to T and store them at yr (S*sizeof(T) = 16 bytes):
+// one 16-byte store when the row allows it, else element stores of the
+// first `valid` pixels.  A failed CTA (bad) stores NaN.
+template <typename T, int S, typename Get>
+__device__ __forceinline__ void mult_store(T *yr, bool full, int valid, bool bad, Get raw_get) {
+    auto get = [&](int i) { return bad ? __int_as_float(0x7fc00000) : raw_get(i); };
+    if (full) {
+        uint32_t u[4];
+        if constexpr (sizeof(T) == 4) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 a = unpack2(u[k], (T *)nullptr);
-            f[2 * k] = a.x; f[2 * k + 1] = a.y;
+            for (int i = 0; i < 4; ++i) u[i] = __float_as_uint(get(i));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[i] = pack2(get(2 * i), get(2 * i + 1), (T *)nullptr);
+        }
+        *reinterpret_cast<uint4 *>(yr) = make_uint4(u[0], u[1], u[2], u[3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < S; ++i)
+            if (i < valid) yr[i] = from_f32<T>(get(i));
+    }
+}
+
+// One block of MB output channels for kMultRT output rows x S pixels of one
+// thread.  brow: the thread's first window in the band (row stride pitch);
+// wsm: weights [kh][kw][m] from the block's first channel; bsm: its bias;
+// yr: output of the block's first channel, first row, first pixel.
+// MB == 4 runs packed fp32x2 FMAs over channel pairs (the weights of two
+// channels against one input value duplicated into both lanes); MB == 1
+// scalar FMAs.  Both round each product-sum to nearest in fp32.
+template <typename T, int SW, int MB, int KWT>
+__device__ __forceinline__ void mult_block(const float *brow, int pitch, int nq, int sh, int KH,
+                                           int KW, const float *wsm, int m, const float *bsm,
+                                           T *yr, int64_t ys1, int64_t ys2, int rows, bool full,
+                                           int valid, bool bad) {
+    constexpr int S = 16 / (int)sizeof(T);
+    constexpr int WL4 = mult_wl4<S, SW, KWT>();
+    constexpr int KWU = KWT ? KWT : kMultMaxKW;
+    constexpr int MP = MB == 4 ? 2 : 1;               // packed channel pairs
+    float2 acc2[kMultRT][MP][S];                      // MB == 4
+    float acc1[kMultRT][S];                           // MB == 1
+    if constexpr (MB == 4) {
+#pragma unroll
+        for (int jp = 0; jp < MP; ++jp) {
+            const float2 bj = make_float2(bsm[2 * jp], bsm[2 * jp + 1]);
+#pragma unroll
+            for (int rr = 0; rr < kMultRT; ++rr)
+#pragma unroll
+                for (int i = 0; i < S; ++i) acc2[rr][jp][i] = bj;
+        }
+    } else {
+#pragma unroll
+        for (int rr = 0; rr < kMultRT; ++rr)
+#pragma unroll
+            for (int i = 0; i < S; ++i) acc1[rr][i] = bsm[0];
+    }
+    for (int qq = 0; qq < nq; ++qq) {
+        // Input row qq of this thread's rows, read once for both output rows.
+        const float4 *src = reinterpret_cast<const float4 *>(brow + qq * pitch);
+        float xr[WL4 * 4];
+#pragma unroll
+        for (int l = 0; l < WL4; ++l) {
+            const float4 v = src[l];
+            xr[4 * l] = v.x; xr[4 * l + 1] = v.y; xr[4 * l + 2] = v.z; xr[4 * l + 3] = v.w;
+        }
+#pragma unroll
+        for (int rr = 0; rr < kMultRT; ++rr) {
+            const int kh = qq - rr * sh;   // kernel row feeding output row rr
+            if (kh < 0 || kh >= KH) continue;
+            const float *wrow = wsm + kh * KW * m;
+#pragma unroll
+            for (int kw = 0; kw < KWU; ++kw) {
+                if (!KWT && kw >= KW) break;
+                if constexpr (MB == 4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(wrow + kw * m);
+                    const float2 w01 = make_float2(t4.x, t4.y), w23 = make_float2(t4.z, t4.w);
+#pragma unroll
+                    for (int i = 0; i < S; ++i) {
+                        const float xv = xr[i * SW + kw];
+                        const float2 xx = make_float2(xv, xv);
+                        acc2[rr][0][i] = __ffma2_rn(w01, xx, acc2[rr][0][i]);
+                        acc2[rr][1][i] = __ffma2_rn(w23, xx, acc2[rr][1][i]);
+                    }
+                } else {
+                    const float wv = wrow[kw * m];
+#pragma unroll
+                    for (int i = 0; i < S; ++i) acc1[rr][i] = fmaf(wv, xr[i * SW + kw], acc1[rr][i]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < kMultRT; ++rr) {
+        if (rr >= rows) break;
+        T *yrow = yr + rr * ys2;
+        if constexpr (MB == 4) {
+#pragma unroll
+            for (int jp = 0; jp < MP; ++jp) {
+                mult_store<T, S>(yrow + (2 * jp) * ys1, full, valid, bad,
+                                 [&](int i) { return acc2[rr][jp][i].x; });
+                mult_store<T, S>(yrow + (2 * jp + 1) * ys1, full, valid, bad,
+                                 [&](int i) { return acc2[rr][jp][i].y; });
+            }
+        } else {
+            mult_store<T, S>(yrow, full, valid, bad, [&](int i) { return acc1[rr][i]; });
         }
     }
 }
 
-}  // namespace gconv
 
-namespace gconv {
-
-template <typename T, int SW, int MB, int MIS>
+template <typename T, int SW, int MB, int KWT>
 __global__ void __launch_bounds__(kMultThreads, kMultCtasPerSM)
-mult_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
-            T *__restrict__ y, Params p, MultGeom g) {
-    constexpr int CE = 16 / (int)sizeof(T);           // elements per 16-byte chunk
-    constexpr int S = CE;                             // output pixels per thread
-    constexpr int WL4 = mult_wl4<S, SW, MIS>();       // 16-byte window loads
-    extern __shared__ __align__(16) float mult_smem[];
-    float *band = mult_smem;                          // rows_in x pitch
-    float *wsm = band + g.rows_in * g.pitch;          // [kh][kw][m]
-    float *bsm = wsm + p.KH * p.KW * g.m;             // [m]
+mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
+            const T *__restrict__ w, const T *__restrict__ b, T *__restrict__ y, Params p,
+            MultGeom g) {
+    constexpr int S = 16 / (int)sizeof(T);            // output pixels per thread
+    extern __shared__ __align__(128) unsigned char mult_smem[];
+    const uint32_t ring = smem_addr(mult_smem);       // raw stage s at ring + s*stage
+    float *band0 = reinterpret_cast<float *>(mult_smem + g.band_off);
+    float *wsm = reinterpret_cast<float *>(mult_smem + g.w_off);   // [kh][kw][m]
+    float *bsm = wsm + p.KH * p.KW * g.m;                          // [m]
+    const uint32_t bars = ring + (uint32_t)g.bar_off;
+    volatile int *failed = reinterpret_cast<volatile int *>(mult_smem + g.bar_off + 16);
+    const int KW = KWT ? KWT : p.KW;
+    const int band_floats = g.rows_in * g.pitch;
 
     const int t = threadIdx.x;
     const int per = g.items / g.ctas, extra = g.items % g.ctas;
@@ -192,79 +289,91 @@ mult_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
     const int i1 = i0 + per + ((int)blockIdx.x < extra ? 1 : 0);
     if (i0 >= i1) return;   // the same for the whole CTA
 
-    // This thread's chunks of a band, fixed for every item: band row in the
-    // high half, chunk index in the low half; -1 when the chunk is unused.
-    int chunk[kMultMaxChunks];
-#pragma unroll
-    for (int k = 0; k < kMultMaxChunks; ++k) {
-        const int q = t + k * kMultThreads;
-        const int br = q / g.cpr;
-        chunk[k] = q < g.nchunks ? (br << 16) | (q - br * g.cpr) : -1;
-    }
-
-    uint4 pre[kMultMaxChunks];
-    // Load the band of `it` into registers: whole 16-byte chunks inside the
-    // row (when rows are 16-byte aligned), element by element at a ragged
-    // edge or on unaligned rows, zeros outside the image.
-    auto fetch = [&](const MultItem &it) {
-        const int ih0 = it.bd * g.BR * p.sh - p.pbh;
-        const int cbase = it.cc * g.OWc * p.sw - p.pbw - g.mis - g.coff;
+    // Box of item `it`: columns from its first window column minus shift,
+    // rows from its first input row.
+    auto box_x = [&](const MultItem &it) { return it.cc * g.OWc * p.sw - p.pbw - g.shift; };
+    auto box_y = [&](const MultItem &it) { return it.bd * g.BR * p.sh - p.pbh; };
+    auto issue = [&](const MultItem &it, int s) {   // one thread
+        const uint32_t bar = bars + 8u * s;
+        mbar_arrive_expect_tx(bar, (uint32_t)g.box_bytes);
+        tma_load_4d(ring + (uint32_t)(s * g.stage), &xmap, bar, box_x(it), box_y(it), it.c, it.n);
+    };
+    // The same box with plain loads (x without a tensor map), zeros outside.
+    auto fill = [&](const MultItem &it, int s) {
+        T *raw = reinterpret_cast<T *>(mult_smem + s * g.stage);
+        const int x0 = box_x(it), y0 = box_y(it);
         const T *plane = x + (int64_t)it.n * p.xs[0] + (int64_t)it.c * p.xs[1];
-#pragma unroll
-        for (int k = 0; k < kMultMaxChunks; ++k) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            const int ih = ih0 + (chunk[k] >> 16);
-            const int col = cbase + (chunk[k] & 0xffff) * CE;
-            if (chunk[k] >= 0 && ih >= 0 && ih < p.H && col + CE > 0 && col < p.W) {
-                const T *row = plane + (int64_t)ih * p.xs[2];
-                if (g.vec_load && col >= 0 && col + CE <= p.W) {
-                    v = __ldg(reinterpret_cast<const uint4 *>(row + col));
-                } else {
-                    union { uint4 u; T e[CE]; } tmp;
-#pragma unroll
-                    for (int e = 0; e < CE; ++e) {
-                        const int cw = col + e;
-                        tmp.e[e] = (cw >= 0 && cw < p.W) ? row[cw] : from_f32<T>(0.f);
-                    }
-                    v = tmp.u;
-                }
-            }
-            pre[k] = v;
-        }
-    };
-    // Widen the fetched chunks into the band: 16-byte shared stores at the
-    // same place for every item (chunk index * CE - coff).
-    auto deposit = [&]() {
-#pragma unroll
-        for (int k = 0; k < kMultMaxChunks; ++k) {
-            if (chunk[k] >= 0) {
-                float f[CE];
-                mult_widen<T>(pre[k], f);
-                const int sc0 = (chunk[k] & 0xffff) * CE - g.coff;
-                float *dst = band + (chunk[k] >> 16) * g.pitch;
-#pragma unroll
-                for (int h = 0; h < CE / 4; ++h) {
-                    const int sc = sc0 + 4 * h;
-                    if (sc >= 0 && sc + 4 <= g.pitch)
-                        *reinterpret_cast<float4 *>(dst + sc) =
-                            make_float4(f[4 * h], f[4 * h + 1], f[4 * h + 2], f[4 * h + 3]);
-                }
-            }
+        for (int e = t; e < g.rows_in * g.BWX; e += kMultThreads) {
+            const int r = e / g.BWX, col = e - r * g.BWX;
+            const int ih = y0 + r, iw = x0 + col;
+            T v = from_f32<T>(0.f);
+            if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) v = plane[(int64_t)ih * p.xs[2] + iw];
+            raw[e] = v;
         }
     };
 
-    const int trow = t / g.PGn, pg = t - trow * g.PGn;
-    const bool thread_on = trow < g.TR;
-    const float *brow0 = band + trow * kMultRT * p.sh * g.pitch + pg * S * SW;
-    const int nq = (kMultRT - 1) * p.sh + p.KH;       // input rows a thread reads
+    // Widening pass: band slot (r, f) = box row r, columns shift + 4f ... + 3.
+    // Slots are dealt round-robin; each thread steps its slot without
+    // divisions.
+    const int slot_dr = kMultThreads / g.spr, slot_df = kMultThreads - slot_dr * g.spr;
+    const int slot_r0 = t / g.spr, slot_f0 = t - slot_r0 * g.spr;
+    auto widen_box = [&](int s, float *band) {
+        const T *raw = reinterpret_cast<const T *>(mult_smem + s * g.stage) + g.shift;
+        int r = slot_r0, f = slot_f0;
+        while (r < g.rows_in) {
+            const T *src = raw + r * g.BWX + 4 * f;
+            *reinterpret_cast<float4 *>(band + r * g.pitch + 4 * f) =
+                make_float4(Elem<T>::to_f32(src[0]), Elem<T>::to_f32(src[1]),
+                            Elem<T>::to_f32(src[2]), Elem<T>::to_f32(src[3]));
+            f += slot_df;
+            r += slot_dr;
+            if (f >= g.spr) { f -= g.spr; ++r; }
+        }
+    };
 
     MultItem item;
     item.set(i0, g, p.N);
-    fetch(item);
+    MultItem ahead = item;   // the item two places further on
+    ahead.next(g, p.N);
+    if (t == 0) {
+        *failed = 0;
+        if (g.use_tma) {
+            tma_prefetch_map(&xmap);
+            mbar_init(bars, 1);
+            mbar_init(bars + 8u, 1);
+            fence_barrier_init();
+            issue(item, 0);
+            if (i0 + 1 < i1) issue(ahead, 1);
+        }
+    }
+    ahead.next(g, p.N);
+    __syncthreads();
+
+    const int trow = t / g.PGn, pg = t - trow * g.PGn;
+    const bool thread_on = trow < g.TR;
+    const int brow_off = trow * kMultRT * p.sh * g.pitch + pg * S * SW;
+    const int nq = (kMultRT - 1) * p.sh + p.KH;       // band rows a thread reads
+
     int cur_c = -1;
-    for (int it = i0; it < i1; ++it) {
-        deposit();
+    int drain = 0;              // stages whose wait gave up
+    uint32_t drain_par[2] = {0u, 0u};
+    for (int it = i0, k = 0; it < i1; ++it, ++k) {
+        const int s = k & 1;
+        float *band = band0 + s * band_floats;
+        if (g.use_tma) {
+            const uint32_t par = (uint32_t)((k >> 1) & 1);
+            if (!mbar_wait(bars + 8u * s, par)) {
+                *failed = 1;
+                drain |= 1 << s;
+                drain_par[s] = par;
+            }
+        } else {
+            fill(item, s);
+            __syncthreads();
+        }
+        widen_box(s, band);
         if (item.c != cur_c) {
+            if (cur_c >= 0) __syncthreads();   // the previous item is done with wsm
             cur_c = item.c;
             const int nw = g.m * p.KH * p.KW;
             for (int e = t; e < nw; e += kMultThreads) {
@@ -276,130 +385,82 @@ mult_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
             for (int j = t; j < g.m; j += kMultThreads)
                 bsm[j] = p.has_bias ? load_f32(b + (int64_t)(cur_c * g.m + j) * p.bs) : 0.f;
         }
-        __syncthreads();
-        MultItem nxt = item;
-        nxt.next(g, p.N);
-        if (it + 1 < i1) fetch(nxt);   // in flight while this band is computed
+        __syncthreads();   // band and weights ready; raw stage s is free
+        // Refill stage s two items ahead (not after a failed wait).
+        if (g.use_tma && t == 0 && it + 2 < i1 && !*failed) issue(ahead, s);
+        ahead.next(g, p.N);
+        const bool bad = *failed != 0;
 
         const int oh0 = item.bd * g.BR + trow * kMultRT;
         const int ow0 = item.cc * g.OWc + pg * S;
         if (thread_on && oh0 < p.OH && ow0 < p.OW) {
-            for (int mb = 0; mb < g.m; mb += MB) {
-                float acc[kMultRT][MB][S];
-#pragma unroll
-                for (int j = 0; j < MB; ++j) {
-                    const float bj = bsm[mb + j];
-#pragma unroll
-                    for (int rr = 0; rr < kMultRT; ++rr)
-#pragma unroll
-                        for (int i = 0; i < S; ++i) acc[rr][j][i] = bj;
-                }
-                for (int qq = 0; qq < nq; ++qq) {
-                    // Input row qq of this thread's rows, read once.
-                    const float4 *src = reinterpret_cast<const float4 *>(brow0 + qq * g.pitch);
-                    float xr[WL4 * 4];
-#pragma unroll
-                    for (int l = 0; l < WL4; ++l) {
-                        const float4 v = src[l];
-                        xr[4 * l] = v.x; xr[4 * l + 1] = v.y; xr[4 * l + 2] = v.z; xr[4 * l + 3] = v.w;
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < kMultRT; ++rr) {
-                        const int kh = qq - rr * p.sh;   // kernel row feeding output row rr
-                        if (kh >= 0 && kh < p.KH) {
-                            const float *wrow = wsm + kh * p.KW * g.m + mb;
-#pragma unroll
-                            for (int kw = 0; kw < kMultMaxKW; ++kw) {
-                                if (kw < p.KW) {
-                                    float wv[MB];
-                                    if constexpr (MB == 4) {
-                                        const float4 t4 = *reinterpret_cast<const float4 *>(wrow + kw * g.m);
-                                        wv[0] = t4.x; wv[1] = t4.y; wv[2] = t4.z; wv[3] = t4.w;
-                                    } else {
-#pragma unroll
-                                        for (int j = 0; j < MB; ++j) wv[j] = wrow[kw * g.m + j];
-                                    }
-#pragma unroll
-                                    for (int j = 0; j < MB; ++j)
-#pragma unroll
-                                        for (int i = 0; i < S; ++i)
-                                            acc[rr][j][i] =
-                                                fmaf(wv[j], xr[MIS + i * SW + kw], acc[rr][j][i]);
-                                }
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int rr = 0; rr < kMultRT; ++rr) {
-                    const int oh = oh0 + rr;
-                    if (oh >= p.OH) continue;
-#pragma unroll
-                    for (int j = 0; j < MB; ++j) {
-                        T *yrow = y + (int64_t)item.n * p.ys[0] +
-                                  (int64_t)(item.c * g.m + mb + j) * p.ys[1] +
-                                  (int64_t)oh * p.ys[2] + ow0;
-                        if (g.vec_store && ow0 + S <= p.OW) {
-                            union { uint4 u; T e[S]; } o;
-#pragma unroll
-                            for (int i = 0; i < S; ++i) o.e[i] = from_f32<T>(acc[rr][j][i]);
-                            *reinterpret_cast<uint4 *>(yrow) = o.u;
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < S; ++i)
-                                if (ow0 + i < p.OW) yrow[i] = from_f32<T>(acc[rr][j][i]);
-                        }
-                    }
-                }
-            }
+            T *ybase = y + (int64_t)item.n * p.ys[0] + (int64_t)(item.c * g.m) * p.ys[1] +
+                       (int64_t)oh0 * p.ys[2] + ow0;
+            const bool full = g.vec_store && ow0 + S <= p.OW;
+            const int rows = p.OH - oh0 < kMultRT ? p.OH - oh0 : kMultRT;
+            for (int mb = 0; mb < g.m; mb += MB)
+                mult_block<T, SW, MB, KWT>(band + brow_off, g.pitch, nq, p.sh, p.KH, KW, wsm + mb,
+                                           g.m, bsm + mb, ybase + (int64_t)mb * p.ys[1], p.ys[1],
+                                           p.ys[2], rows, full, p.OW - ow0, bad);
         }
-        __syncthreads();   // the band and weights are rewritten for the next item
-        item = nxt;
+        item.next(g, p.N);
     }
+    // A box whose wait gave up may still land: wait for it once more
+    // (bounded) before the CTA's shared memory is released.
+    for (int st = 0; st < 2; ++st)
+        if (drain & (1 << st)) (void)mbar_wait(bars + 8u * st, drain_par[st]);
 }
 
-// Host launcher for one dtype: geometry, output-store alignment, template
-// choice (column stride, multiplier blocking, window offset).
-template <typename T, int SW, int MB, int MIS>
-cudaError_t mult_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const MultGeom &g) {
-    const size_t smem = mult_smem_bytes(p, g);
-    cudaError_t e = cudaFuncSetAttribute(mult_kernel<T, SW, MB, MIS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+// Host launcher for one dtype: geometry, tensor map (or plain fills),
+// output-store alignment, template choice (column stride, multiplier
+// blocking, kernel width).
+template <typename T, int SW, int MB, int KWT>
+cudaError_t mult_launch_t(const CUtensorMap &map, const Params &p, const Ptrs &q, cudaStream_t s,
+                          const MultGeom &g) {
+    cudaError_t e = cudaFuncSetAttribute(mult_kernel<T, SW, MB, KWT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
-    mult_kernel<T, SW, MB, MIS><<<g.ctas, kMultThreads, smem, s>>>(
-        static_cast<const T *>(q.x), static_cast<const T *>(q.w), static_cast<const T *>(q.b),
-        static_cast<T *>(q.y), p, g);
+    mult_kernel<T, SW, MB, KWT><<<g.ctas, kMultThreads, g.smem, s>>>(
+        map, static_cast<const T *>(q.x), static_cast<const T *>(q.w),
+        static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
     return cudaGetLastError();
 }
 
-template <typename T, int SW, int MB>
-cudaError_t mult_launch_mis(const Params &p, const Ptrs &q, cudaStream_t s, const MultGeom &g) {
-    switch (g.mis) {
-    case 0: return mult_launch_t<T, SW, MB, 0>(p, q, s, g);
-    case 1: return mult_launch_t<T, SW, MB, 1>(p, q, s, g);
-    case 2: return mult_launch_t<T, SW, MB, 2>(p, q, s, g);
-    case 3: return mult_launch_t<T, SW, MB, 3>(p, q, s, g);
+template <typename T, int MB>
+cudaError_t mult_launch_kw(const CUtensorMap &map, const Params &p, const Ptrs &q, cudaStream_t s,
+                           const MultGeom &g) {
+    if (p.sw == 2) return mult_launch_t<T, 2, MB, 0>(map, p, q, s, g);
+    switch (p.KW) {
+    case 3: return mult_launch_t<T, 1, MB, 3>(map, p, q, s, g);
+    case 4: return mult_launch_t<T, 1, MB, 4>(map, p, q, s, g);
+    case 5: return mult_launch_t<T, 1, MB, 5>(map, p, q, s, g);
+    case 7: return mult_launch_t<T, 1, MB, 7>(map, p, q, s, g);
     }
-    return cudaErrorInvalidValue;
+    return mult_launch_t<T, 1, MB, 0>(map, p, q, s, g);
 }
 
 template <typename T>
 cudaError_t mult_launch_dtype(const Params &p, const Ptrs &q, cudaStream_t s) {
     MultGeom g;
     if (!mult_geometry(p, sizeof(T), g)) return cudaErrorNotSupported;
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(q.x);
-    g.vec_load = (xa % 16 == 0) && ((p.xs[2] * (int64_t)sizeof(T)) % 16 == 0) &&
-                 ((p.xs[1] * (int64_t)sizeof(T)) % 16 == 0) &&
-                 ((p.xs[0] * (int64_t)sizeof(T)) % 16 == 0);
+    const int64_t es = sizeof(T);
+    CUtensorMap map{};
+    const bool tma_ok = reinterpret_cast<uintptr_t>(q.x) % 16 == 0 && (p.xs[2] * es) % 16 == 0 &&
+                        (p.xs[1] * es) % 16 == 0 && (p.xs[0] * es) % 16 == 0;
+    if (tma_ok) {
+        // x as (W, H, C, N), innermost first; a box is one item's band.
+        const uint64_t dims[4] = {(uint64_t)p.W, (uint64_t)p.H, (uint64_t)p.C_in, (uint64_t)p.N};
+        const uint64_t strides[3] = {(uint64_t)(p.xs[2] * es), (uint64_t)(p.xs[1] * es),
+                                     (uint64_t)(p.xs[0] * es)};
+        const uint32_t box[4] = {(uint32_t)g.BWX, (uint32_t)g.rows_in, 1u, 1u};
+        g.use_tma = tma_encode_4d(&map, tma_dtype<T>(), q.x, dims, strides, box) ? 1 : 0;
+    }
     // 16-byte output stores need 16-byte aligned rows
     const uintptr_t ya = reinterpret_cast<uintptr_t>(q.y);
-    g.vec_store = (ya % 16 == 0) && ((p.ys[2] * (int64_t)sizeof(T)) % 16 == 0) &&
-                  ((p.ys[1] * (int64_t)sizeof(T)) % 16 == 0) &&
-                  ((p.ys[0] * (int64_t)sizeof(T)) % 16 == 0) && p.ys[3] == 1;
-    const bool mb4 = g.m % 4 == 0;
-    if (p.sw == 1)
-        return mb4 ? mult_launch_mis<T, 1, 4>(p, q, s, g) : mult_launch_mis<T, 1, 1>(p, q, s, g);
-    return mb4 ? mult_launch_mis<T, 2, 4>(p, q, s, g) : mult_launch_mis<T, 2, 1>(p, q, s, g);
+    g.vec_store = (ya % 16 == 0) && ((p.ys[2] * es) % 16 == 0) && ((p.ys[1] * es) % 16 == 0) &&
+                  ((p.ys[0] * es) % 16 == 0) && p.ys[3] == 1;
+    return g.m % 4 == 0 ? mult_launch_kw<T, 4>(map, p, q, s, g)
+                        : mult_launch_kw<T, 1>(map, p, q, s, g);
 }
 
 cudaError_t mult_launch_f32(const Params &p, const Ptrs &q, cudaStream_t s);

@@ -375,12 +375,6 @@ bool row8_geometry(const Params &p, Row8Geom &g) {
     return true;
 }
 
-template <typename T> constexpr CUtensorMapDataType tma_dtype() {
-    return sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                          : (std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-}
-
 template <typename T, int K, int SH>
 cudaError_t row8_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
     constexpr int VEC = row8_vec<T>(K);

@@ -16,6 +16,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <type_traits>
 
 namespace gconv {
 
@@ -27,6 +29,13 @@ constexpr uint32_t kTmaSpinLimit = 1u << 26;
 bool tma_encode_4d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
                    const uint64_t dims[4], const uint64_t strides_bytes[3],
                    const uint32_t box[4]);
+
+// Tensor-map element type of T (float, __half or __nv_bfloat16).
+template <typename T> constexpr CUtensorMapDataType tma_dtype() {
+    return sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                          : (std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
