@@ -26,9 +26,10 @@
 //  - Accumulators start at the bias (fp32); a finished output row is
 //    rounded once to the output dtype and stored with coalesced 4/8/16-byte
 //    stores through a pointer that advances one output row at a time.
-//  - A wait that gives up (it should never happen) marks the CTA failed;
-//    from then on its outputs are written as NaN, so the failure is visible
-//    in the result instead of hanging the GPU.
+//  - A wait that gives up (it should never happen) poisons the waiting
+//    thread's accumulators and bias with NaN, so from then on its outputs
+//    are NaN: the failure is visible in the result instead of hanging the
+//    GPU, and the store path carries no per-value check.
 #pragma once
 
 #include "gconv_internal.h"
@@ -89,6 +90,8 @@ __device__ __forceinline__ Row8Run row8_run_at(int u, int o1, int OH, int CC, in
     return r;
 }
 
+constexpr float kNaN = __builtin_nanf("");
+
 // Floor division and modulo for compile-time constants (may be negative).
 constexpr int fdiv(int a, int b) { return (a >= 0) ? a / b : -((-a + b - 1) / b); }
 constexpr int fmod_pos(int a, int b) { return ((a % b) + b) % b; }
@@ -143,14 +146,13 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
 
     const uint32_t ring = smem_addr(row8_ring);
     const uint32_t bars = ring + (uint32_t)(g.NS * g.stage);   // NS mbarriers
-    volatile int *failed = reinterpret_cast<volatile int *>(row8_ring + g.NS * g.stage + 8 * g.NS);
     // fp32 weights [tap][chunk channel] and bias, after the barriers
     float *wsm = reinterpret_cast<float *>(row8_ring + g.NS * g.stage + 8 * g.NS + 16);
     const int row_bytes = g.Win * g.pitch;       // one staged input row
 
     // Producer (thread 0 only): the run and stage of the next box.  A stage
     // holds U consecutive input rows of one run.
-    Row8Run prun;
+    Row8Run prun{};
     int pnext_u = 0, pst = 0, pnst = 0, pslot = 0;
     bool pdone = false;
     auto issue = [&]() {
@@ -221,7 +223,6 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     if (t == 0) {
         tma_prefetch_map(&xmap);
         for (int i = 0; i < g.NS; ++i) mbar_init(bars + 8u * i, 1);
-        *failed = 0;
         fence_barrier_init();
         prun = row8_run_at<K, SH>(o0, o1, p.OH, g.CC, g.HC);
         pnext_u = o0 + prun.rows;
@@ -234,6 +235,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     int cslot = 0;        // stage of the consumer's next box
     uint32_t cphase = 0;  // parity of that stage's current use
 
+    bool bad = false;     // a box wait gave up (outputs become NaN)
     int u = o0;
     while (u < o1) {
         const Row8Run run = row8_run_at<K, SH>(u, o1, p.OH, g.CC, g.HC);
@@ -246,6 +248,9 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             stage_weights(loaded_hc);
             __syncthreads();
             take_weights();
+            if (bad)
+#pragma unroll
+                for (int k = 0; k < P; ++k) bias[k] = make_float2(kNaN, kNaN);
         }
         // Accumulator set s serves the output rows j with j mod R == s; it
         // is reset to the bias right after its row's last input row.
@@ -258,13 +263,29 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
                 for (int k = 0; k < P; ++k) acc[s][i][k] = bias[k];
 
         const int ow0 = run.cc * g.OWc + pg * S;
-        // the run's first output row at this thread's pixels and channels
-        T *ynext = y + (int64_t)run.n * p.ys[0] + (int64_t)run.oh0 * p.ys[2] +
-                   (int64_t)ow0 * p.ys[3] + (active ? c0 : 0);
+        // output row r0 / SH of the run at this thread's pixels and channels
+        T *ystage = y + (int64_t)run.n * p.ys[0] + (int64_t)run.oh0 * p.ys[2] +
+                    (int64_t)ow0 * p.ys[3] + (active ? c0 : 0);
+        bool pix_ok[S];
+#pragma unroll
+        for (int i = 0; i < S; ++i) pix_ok[i] = ow0 + i < p.OW;
         const uint32_t win0 = ring + (uint32_t)(cvl * VB + pg * S * SW * g.pitch);
 
         for (int r0 = 0; r0 < run.nin; r0 += U) {
-            if (!mbar_wait(bars + 8u * cslot, cphase)) *failed = 1;
+            if (!mbar_wait(bars + 8u * cslot, cphase)) {
+                // The box did not arrive: poison every open accumulator and
+                // the bias, so every output this thread stores from now on
+                // is NaN (the bias is poisoned again after a weight reload).
+                bad = true;
+#pragma unroll
+                for (int s = 0; s < R; ++s)
+#pragma unroll
+                    for (int i = 0; i < S; ++i)
+#pragma unroll
+                        for (int k = 0; k < P; ++k) acc[s][i][k] = make_float2(kNaN, kNaN);
+#pragma unroll
+                for (int k = 0; k < P; ++k) bias[k] = make_float2(kNaN, kNaN);
+            }
             const uint32_t stage0 = win0 + (uint32_t)(cslot * g.stage);
             // Straight-line over the stage's U rows (no branches around the
             // arithmetic, so the scheduler can overlap the rows' loads):
@@ -304,20 +325,12 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
                     const int set = fmod_pos(fdiv(d, SH), R);
                     const int jn = r - (K - 1);          // SH * output row within the run
                     if (active && jn >= 0 && jn < run.rows * SH) {
-                        const bool bad = *failed != 0;
-                        T *yrow = ynext + (int64_t)(jn / SH) * p.ys[2];
+                        // output row jn / SH = r0 / SH + (ph - K + 1) / SH
+                        T *yrow = ystage + (int64_t)fdiv(ph - (K - 1), SH) * p.ys[2];
 #pragma unroll
-                        for (int i = 0; i < S; ++i) {
-                            if (ow0 + i < p.OW) {
-                                float2 o[P];
-#pragma unroll
-                                for (int k = 0; k < P; ++k)
-                                    o[k] = bad ? make_float2(__int_as_float(0x7fc00000),
-                                                             __int_as_float(0x7fc00000))
-                                               : acc[set][i][k];
-                                IO::store(yrow + (int64_t)i * p.ys[3], pack_pairs<T, VEC>(o));
-                            }
-                        }
+                        for (int i = 0; i < S; ++i)
+                            if (pix_ok[i])
+                                IO::store(yrow + (int64_t)i * p.ys[3], pack_pairs<T, VEC>(acc[set][i]));
                     }
 #pragma unroll
                     for (int i = 0; i < S; ++i)
@@ -325,6 +338,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
                         for (int k = 0; k < P; ++k) acc[set][i][k] = bias[k];
                 }
             }
+            ystage += (int64_t)R * p.ys[2];   // U / SH output rows per stage
             if (++cslot == g.NS) {
                 cslot = 0;
                 cphase ^= 1u;
