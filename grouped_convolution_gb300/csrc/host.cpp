@@ -224,7 +224,7 @@ gconv_status out_shape_and_stride(const gconv_desc *d, int32_t *rank,
 }
 
 // The per-shape picker.  Specialised schedules win where they apply; the
-// portable base takes everything else.  Calls with too few outputs to give
+// fallback schedule dw_flat takes everything else.  Calls with too few outputs to give
 // every thread of the GPU its own (fewer than 152 SMs x 512) and a long tap
 // loop split the taps across lanes instead.
 static int32_t pick(const gconv_desc &d, const Ptrs &p) {

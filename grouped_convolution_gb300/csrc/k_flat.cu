@@ -1,5 +1,5 @@
-// k_flat.cu -- dw_flat, the portable base schedule (executorch PR #25085,
-// description, second paragraph: "the portable base").
+// k_flat.cu -- dw_flat, the schedule that takes every call (executorch PR
+// #25085, description, second paragraph, names it as the fallback).
 //
 // One thread per output element, threads numbered in y's memory order so
 // stores are coalesced in either layout.  x, w and bias are read through

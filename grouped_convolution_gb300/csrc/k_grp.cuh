@@ -1,7 +1,7 @@
 // k_grp.cuh -- grp_plane: few-channel grouped convolution (1 <= Cin_g <= 8)
 // with the group's weights shared by a whole CTA (executorch PR #25085,
-// description, second paragraph: "grp_plane, one output channel per program
-// with shared weights").
+// description, second paragraph, names this schedule: each program computes
+// one output channel and the group's weights are shared).
 //
 // Design for sm_103a:
 //  - A CTA owns one (image, group, TR x TC*P output tile); the grid runs the

@@ -1,8 +1,7 @@
 // k_mult.cuh -- dw_mult: depthwise convolution with a channel multiplier
 // m <= 16 on NCHW input, every output channel of an input channel computed
 // from one load of that input channel (executorch PR #25085, description,
-// second paragraph: all output channels of an input channel per load, for
-// multipliers up to 16).
+// second paragraph, names this schedule and its multiplier bound of 16).
 //
 // Design for sm_103a:
 //  - Work items are (input channel c, image n, band of BR output rows,

@@ -1,6 +1,7 @@
 // k_reduce.cu -- grp_reduce: a parallel reduction over the taps for
 // convolutions with few outputs (executorch PR #25085, description, second
-// paragraph: "grp_reduce, a parallel reduction over taps for few outputs").
+// paragraph, names this schedule: the taps of one output are summed in
+// parallel, for calls with few outputs).
 //
 // Each output element is shared by L lanes of a warp (L = 8, or 32 when the
 // tap count Cin_g*KH*KW is large): lane l accumulates taps l, l+L, l+2L, ...

@@ -1,6 +1,7 @@
-// k_row8.cuh -- dw_row8: channels-last depthwise (multiplier 1) with a
-// register sliding window (executorch PR #25085, description, second
-// paragraph: "a register sliding window for channel-contiguous inputs").
+// k_row8.cuh -- dw_row8: channels-last depthwise (multiplier 1) whose input
+// window slides through registers (executorch PR #25085, description,
+// second paragraph, names this schedule for inputs whose channels are
+// contiguous).
 //
 // Design for sm_103a (one persistent pass over HBM):
 //  - Work is a flat list of output rows u = ((n*CC + cc)*HC + hc)*OH + oh
@@ -49,7 +50,11 @@ constexpr int row8_vec(int K) {
 // Output pixels per thread and the CTA size cap, which sets how many
 // registers a thread may use (weights + R*S accumulator pairs + window).
 constexpr int row8_s(int K) { return K == 5 ? 4 : 2; }
-constexpr int row8_max_threads(int K) { return K <= 3 ? 512 : (K <= 5 ? 384 : 336); }
+constexpr int row8_max_threads(int K) { return K <= 3 ? 256 : (K <= 5 ? 384 : 336); }
+// Persistent CTAs per SM (their shared memory splits the SM's).  Measured on
+// the 3x3 layers: two 256-thread CTAs overlap one another's barrier and
+// wait phases and beat one 512-thread CTA; three are slower.
+constexpr int row8_ctas_per_sm(int K) { return K <= 3 ? 2 : 1; }
 constexpr int kRow8MaxStages = 8;
 // Input rows per stage: one rotation period of the accumulator sets.
 constexpr int row8_rows_per_stage(int K, int SH) { return SH * ((K + SH - 1) / SH); }
@@ -117,7 +122,7 @@ template <> struct Lds<16> {
 };
 
 template <typename T, int K, int SH>
-__global__ void __launch_bounds__(row8_max_threads(K), 1)
+__global__ void __launch_bounds__(row8_max_threads(K), row8_ctas_per_sm(K))
 row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             const T *__restrict__ w, const T *__restrict__ b, T *__restrict__ y, Params p,
             Row8Geom g) {
@@ -378,14 +383,15 @@ bool row8_geometry(const Params &p, Row8Geom &g) {
     g.pitch = g.CVc * VB;
     g.box_bytes = g.Win * g.pitch * row8_rows_per_stage(K, p.sh);
     g.stage = (g.box_bytes + 127) / 128 * 128;
-    int ns = (200 * 1024 - (K * K + 1) * g.CVc * VEC * 4) / g.stage;
+    int ns = (200 * 1024 / row8_ctas_per_sm(K) - (K * K + 1) * g.CVc * VEC * 4) / g.stage;
     if (ns > kRow8MaxStages) ns = kRow8MaxStages;
     if (ns < 2) return false;
     g.NS = ns;
     const int64_t units = (int64_t)p.N * g.CC * g.HC * p.OH;
     if (units > INT32_MAX / 2) return false;
     g.units = (int)units;
-    g.ctas = g.units < 152 ? g.units : 152;   // one persistent CTA per SM
+    const int cap = 152 * row8_ctas_per_sm(K);   // persistent CTAs
+    g.ctas = g.units < cap ? g.units : cap;
     return true;
 }
 

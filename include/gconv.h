@@ -81,7 +81,7 @@ typedef enum gconv_status {
  * picker choose. */
 typedef enum gconv_schedule {
     GCONV_SCHED_AUTO = -1,
-    GCONV_SCHED_DW_FLAT = 0,     /* portable base: any layout, multiplier and group shape */
+    GCONV_SCHED_DW_FLAT = 0,     /* fallback: any layout, multiplier and group shape */
     GCONV_SCHED_DW_ROW8 = 1,     /* channels-last depthwise: 16-byte channel vectors,
                                     register sliding window down the rows */
     GCONV_SCHED_DW_MULT = 2,     /* depthwise, multiplier <= 16: every output channel of an
