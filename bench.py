@@ -178,11 +178,12 @@ class ClockSampler:
 # Source files that define each schedule's kernel; the recorded DRAM traffic
 # of a kernel is void once any of them changes.
 KERNEL_SOURCES = {
-    "dw_row8": ["k_row8.cuh", "k_row8.cu", "stencil_math.cuh", "device_common.cuh"],
+    "dw_row8": ["k_row8.cuh", "k_row8.cu", "stencil_math.cuh", "device_common.cuh", "tma.cuh"],
     "dw_flat": ["k_flat.cu", "device_common.cuh"],
-    "dw_mult": ["k_mult.cu", "device_common.cuh"],
+    "dw_mult": ["k_mult.cuh", "k_mult.cu", "device_common.cuh", "tma.cuh"],
     "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh"],
     "grp_reduce": ["k_reduce.cu", "device_common.cuh"],
+    "grp_tc": ["k_tc.cu", "device_common.cuh", "tma.cuh"],
 }
 
 

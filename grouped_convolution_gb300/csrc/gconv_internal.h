@@ -46,6 +46,7 @@ extern const Schedule kDwRow8;
 extern const Schedule kDwMult;
 extern const Schedule kGrpPlane;
 extern const Schedule kGrpReduce;
+extern const Schedule kGrpTc;
 
 inline bool aligned(const void *p, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;

@@ -28,7 +28,7 @@ std::atomic<uint64_t> g_launches{0};
 thread_local int32_t t_last_cuda_error = 0;
 
 const Schedule *const kSchedules[GCONV_SCHED_COUNT] = {
-    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce};
+    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc};
 
 int32_t schedule_from_string(const char *s) {
     if (!s || !*s) return GCONV_SCHED_AUTO;
@@ -224,13 +224,16 @@ gconv_status out_shape_and_stride(const gconv_desc *d, int32_t *rank,
 }
 
 // The per-shape picker.  Specialised schedules win where they apply; the
-// fallback schedule dw_flat takes everything else.  Calls with too few outputs to give
-// every thread of the GPU its own (fewer than 152 SMs x 512) and a long tap
-// loop split the taps across lanes instead.
+// fallback schedule dw_flat takes everything else.  Grouped calls the
+// tensor cores can take (4 or 8 channels per group, channels-last 16-bit)
+// run there.  Other calls with too few outputs to give every thread of the
+// GPU its own (fewer than 152 SMs x 512) and a long tap loop split the taps
+// across lanes instead.
 static int32_t pick(const gconv_desc &d, const Ptrs &p) {
     const bool dw = d.Cin_g == 1;
     if (dw && d.Cout_g == 1 && kDwRow8.supports(d, p)) return GCONV_SCHED_DW_ROW8;
     if (dw && kDwMult.supports(d, p)) return GCONV_SCHED_DW_MULT;
+    if (!dw && kGrpTc.supports(d, p)) return GCONV_SCHED_GRP_TC;
     const double outputs = (double)d.N * d.C_out * d.OH * d.OW;
     const int64_t taps = d.Cin_g * d.KH * d.KW;
     if (outputs < 152.0 * 512 && taps >= 32) return GCONV_SCHED_GRP_REDUCE;

@@ -90,7 +90,10 @@ typedef enum gconv_schedule {
                                     weights shared in shared memory */
     GCONV_SCHED_GRP_REDUCE = 4,  /* grouped, few outputs: taps split across the lanes of a
                                     warp and reduced with shuffles */
-    GCONV_SCHED_COUNT = 5
+    GCONV_SCHED_GRP_TC = 5,      /* grouped, 4 or 8 channels per group, channels-last bf16 /
+                                    fp16: implicit GEMM on the tcgen05 tensor cores, fp32
+                                    accumulation in tensor memory */
+    GCONV_SCHED_COUNT = 6
 } gconv_schedule;
 
 typedef enum gconv_layout {

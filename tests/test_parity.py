@@ -49,7 +49,7 @@ GEOMS = [
 ]
 
 DTYPES = ["f32", "f16", "bf16"]
-SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce"]
+SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc"]
 
 
 def workload(g, dtype, cl, bias, seed):
@@ -151,6 +151,32 @@ def test_dw_mult_geometry_matches_oracle(case, dtype):
     y = run_gpu(wl, x, w, b, "dw_mult")
     assert y is not None, "dw_mult must take this case"
     RAN["dw_mult"] += 1
+    check(wl, x, w, b, y)
+
+
+# grp_tc (tensor-core implicit GEMM) tile geometry: several 64-pixel column
+# tiles and a ragged last tile, row blocks shorter than a unit, 4 and 8
+# input channels per group, 8 / 16 / 32 output channels per 8-channel
+# chunk, strides 1 to 3, kernels from 1x1 to 9x9, asymmetric padding.
+TC_CASES = [
+    # name, N, Cin_g, Cout_g, G, H, W, KH, KW, stride, pad_before, pad_after
+    ("c5_small", 1, 4, 8, 4, 33, 40, 9, 9, (2, 2), (4, 4), (4, 4)),
+    ("wide_s1", 1, 4, 4, 2, 7, 150, 3, 3, (1, 1), (1, 1), (1, 1)),
+    ("cin8_k5x4", 2, 8, 8, 2, 12, 70, 5, 4, (1, 2), (2, 1), (2, 2)),
+    ("cout16_s3", 1, 4, 16, 2, 10, 66, 3, 5, (3, 1), (0, 2), (1, 2)),
+    ("k1", 1, 8, 16, 1, 5, 9, 1, 1, (1, 1), (0, 0), (0, 0)),
+    ("k9x7_ragged", 1, 4, 8, 2, 20, 129, 9, 7, (2, 2), (4, 3), (4, 3)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("case", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_grp_tc_geometry_matches_oracle(case, dtype):
+    wl = workload(case, dtype, True, TC_CASES.index(case) % 2 == 0, seed=61 + TC_CASES.index(case))
+    x, w, b = make_inputs(wl)
+    y = run_gpu(wl, x, w, b, "grp_tc")
+    assert y is not None, "grp_tc must take this case"
+    RAN["grp_tc"] += 1
     check(wl, x, w, b, y)
 
 
