@@ -44,7 +44,8 @@
 namespace gconv {
 namespace {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcProducers = 128;   // warps 0-3: staging and TMEM drain
+constexpr int kTcThreads = 160;     // + warp 4: MMA issue
 constexpr int kTcMT = 64;          // output pixels per tile (MMA M)
 constexpr int kTcMaxMMA = 48;      // tap pairs per output row (9x9: 45)
 constexpr int kTcSmemCap = 112 * 1024;   // two CTAs per SM
@@ -61,7 +62,7 @@ struct TcGeom {
     int nmma;       // MMAs (tap pairs) per output row
     int tap[kTcMaxMMA];   // kh | phase << 4 | s0 << 8 | kw0 << 12 | kw1 << 16 (kw1 15: none)
     int a_off[2];   // shared-memory byte offsets
-    int b_off, tab_off, bar_off, smem;
+    int b_off, tab_off, bias_off, bar_off, smem;
     int stage_bytes, b_sbo;   // A stage bytes, B stride between 8-row groups
     int tmem_cols;
     int units, ctas;
@@ -117,8 +118,9 @@ bool tc_geometry(const Params &p, TcGeom &g) {
     g.a_off[1] = (g.stage_bytes + 1023) / 1024 * 1024;
     g.b_off = g.a_off[1] + (g.stage_bytes + 1023) / 1024 * 1024;
     g.tab_off = g.b_off + (b_bytes + 127) / 128 * 128;
-    g.bar_off = g.tab_off + kTcMaxMMA * 4;
-    g.smem = g.bar_off + 32;   // two mbarriers, TMEM address slot
+    g.bias_off = g.tab_off + kTcMaxMMA * 4;
+    g.bar_off = g.bias_off + 2 * 32 * 4;
+    g.smem = g.bar_off + 64;   // six mbarriers, TMEM address slot, failure flag
     if (g.smem > kTcSmemCap) return false;
     int cols = 2 * g.R * g.NN, pow2 = 32;
     while (pow2 < cols) pow2 *= 2;
@@ -201,6 +203,33 @@ __device__ __forceinline__ void tc_cp16(uint32_t dst, const void *src, int src_b
                  : "memory");
 }
 
+// Bounded wait on an mbarrier phase.  Gives up (returns false) after
+// kTcSpinLimit polls or as soon as the CTA is marked failed, so one lost
+// arrival never turns into a chain of long waits.
+constexpr uint32_t kTcSpinLimit = 1u << 22;
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int *failed) {
+    for (uint32_t i = 0; i < kTcSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (*failed) return false;
+    }
+    *failed = 1;
+    return false;
+}
+__device__ __forceinline__ void tc_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_producer_sync() {   // warps 0-3 only
+    asm volatile("bar.sync 1, %0;\n" ::"n"(kTcProducers) : "memory");
+}
+
 template <typename T, int SW>
 __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSM)
 tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
@@ -214,18 +243,29 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
     if (nunits <= 0) return;   // the same for the whole CTA
 
     int *atab = reinterpret_cast<int *>(tc_smem + g.tab_off);   // A offsets, 16-byte units
-    const uint32_t bars = sbase + (uint32_t)g.bar_off;            // two mbarriers
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(tc_smem + g.bar_off + 16);
+    float *bias_s = reinterpret_cast<float *>(tc_smem + g.bias_off);   // [2][32]
+    // mbarriers: full[2] (rows + weights staged, 128 arrivals), done[2]
+    // (the unit's MMAs completed, tcgen05.commit), empty[2] (TMEM block
+    // drained, 128 arrivals).
+    const uint32_t bar_full = sbase + (uint32_t)g.bar_off;
+    const uint32_t bar_done = bar_full + 16u;
+    const uint32_t bar_empty = bar_full + 32u;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(tc_smem + g.bar_off + 48);
+    volatile int *failed = reinterpret_cast<volatile int *>(tc_smem + g.bar_off + 52);
     T *bsm = reinterpret_cast<T *>(tc_smem + g.b_off);
 
-    if (warp == 0) tc_alloc(sbase + (uint32_t)(g.bar_off + 16), g.tmem_cols);
+    if (warp == 4) tc_alloc(sbase + (uint32_t)(g.bar_off + 48), g.tmem_cols);
     if (t == 0) {
-        mbar_init(bars, 1);
-        mbar_init(bars + 8u, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_full + 8u * i, kTcProducers);
+            mbar_init(bar_done + 8u * i, 1);
+            mbar_init(bar_empty + 8u * i, kTcProducers);
+        }
+        *failed = 0;
         fence_barrier_init();
     }
-    for (int i = t; i < g.nmma; i += kTcThreads) {
-        const int e = g.tap[i];
+    for (int i = t; i < kTcMaxMMA; i += kTcThreads) {
+        const int e = i < g.nmma ? g.tap[i] : g.tap[0];   // padded entries are never issued
         atab[i] = (((e & 15) * SW + ((e >> 4) & 15)) * g.NJ + ((e >> 8) & 15));
     }
     tc_fence_before();
@@ -233,160 +273,205 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    // Stage the input rows of unit u into A buffer buf (cp.async, 16 bytes
-    // per entry, zero fill outside the image); one commit group.
-    auto stage_a = [&](const TcUnit &u, int buf) {
-        const uint32_t dst0 = sbase + (uint32_t)g.a_off[buf];
-        const int ih0 = u.ob * g.R * p.sh - p.pbh;
-        const int iw0 = u.ot * kTcMT * SW - p.pbw;
-        const T *xc = x + (int64_t)u.n * p.xs[0] + (int64_t)(8 * u.c) * p.xs[1];
-        for (int rp = warp; rp < g.rows_in * SW; rp += kTcThreads / 32) {
-            const int r = rp / SW, ph = rp - r * SW;
-            const int ih = ih0 + r;
-            const bool row_ok = ih >= 0 && ih < p.H;
-            const T *xrow = xc + (int64_t)(row_ok ? ih : 0) * p.xs[2];
-            for (int j = lane; j < g.NJ; j += 32) {
-                const int iw = iw0 + j * SW + ph;
-                const bool ok = row_ok && iw >= 0 && iw < p.W;
-                tc_cp16(dst0 + (uint32_t)((rp * g.NJ + j) * 16),
-                        ok ? (const void *)(xrow + (int64_t)iw * p.xs[3]) : (const void *)x,
-                        ok ? 16 : 0);
+    if (warp == 4) {
+        // ---------------- MMA issuer (one thread) ----------------
+        if (lane == 0) {
+            const uint64_t bdesc0 = tc_desc(sbase + (uint32_t)g.b_off, 128, (uint32_t)g.b_sbo);
+            for (int k = 0; k < nunits; ++k) {
+                const int buf = k & 1;
+                tc_wait(bar_full + 8u * buf, (uint32_t)((k >> 1) & 1), failed);
+                if (k >= 2) tc_wait(bar_empty + 8u * buf, (uint32_t)(((k - 2) >> 1) & 1), failed);
+                tc_fence_after();
+                const uint64_t adesc0 = tc_desc(sbase + (uint32_t)g.a_off[buf], 16, 128);
+                for (int rr = 0; rr < g.R; ++rr) {
+                    const uint32_t d = tmem + (uint32_t)((buf * g.R + rr) * g.NN);
+                    const int rowoff = rr * p.sh * SW * g.NJ;   // 16-byte units
+                    for (int i0 = 0; i0 < g.nmma; i0 += 8) {
+                        int a[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) a[j] = atab[i0 + j];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (i0 + j < g.nmma)
+                                tc_mma(d, adesc0 + (uint64_t)(rowoff + a[j]),
+                                       bdesc0 + (uint64_t)(16 * (i0 + j)), g.idesc, i0 + j);
+                    }
+                }
+                tc_commit(bar_done + 8u * buf);
             }
         }
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
-    };
-    // Stage chunk c's weights into B: row n (output channel c*NN + n),
-    // K slice q = 2*mma + half holds the 8 chunk channels of that tap; the
-    // channels outside n's group (and the missing second tap) are zero.
-    auto stage_b = [&](int c) {
-        const int nq = 2 * g.nmma;
-        const int total = g.NN * nq * 8;
-        for (int e = t; e < total; e += kTcThreads) {
-            const int ci8 = e & 7;
-            const int q = (e >> 3) % nq;
-            const int n = (e >> 3) / nq;
-            const int tp = g.tap[q >> 1];
-            const int kh = tp & 15;
-            const int kw = (q & 1) ? ((tp >> 16) & 15) : ((tp >> 12) & 15);
-            const int co = c * g.NN + n;
-            const int ci = ci8 - (n / p.Cout_g) * p.Cin_g;   // channel within n's group
-            T v = from_f32<T>(0.f);
-            if (kw < p.KW && ci >= 0 && ci < p.Cin_g)
-                v = w[(int64_t)co * p.ws[0] + (int64_t)ci * p.ws[1] + (int64_t)kh * p.ws[2] +
-                      (int64_t)kw * p.ws[3]];
-            bsm[((n >> 3) * g.b_sbo + q * 128 + (n & 7) * 16 + ci8 * 2) / 2] = v;
-        }
-    };
-
-    // Issue unit k's MMAs (one thread): R output rows into TMEM columns
-    // [(buf*R + rr)*NN, +NN), nmma tap pairs each, then commit.
-    const uint64_t bdesc0 = tc_desc(sbase + (uint32_t)g.b_off, 128, (uint32_t)g.b_sbo);
-    auto issue = [&](int buf) {
-        const uint64_t adesc0 = tc_desc(sbase + (uint32_t)g.a_off[buf], 16, 128);
-        for (int rr = 0; rr < g.R; ++rr) {
-            const uint32_t d = tmem + (uint32_t)((buf * g.R + rr) * g.NN);
-            const int rowoff = rr * p.sh * SW * g.NJ;   // 16-byte units
-            for (int i = 0; i < g.nmma; ++i)
-                tc_mma(d, adesc0 + (uint64_t)(rowoff + atab[i]), bdesc0 + (uint64_t)(16 * i),
-                       g.idesc, i);
-        }
-        tc_commit(bars + 8u * (uint32_t)buf);
-    };
-
-    bool bad = false;   // a wait gave up: outputs become NaN
-    // Drain unit u from TMEM buffer buf: warp w holds tile rows 16w..16w+15
-    // in its lanes 0-15 (the M = 64 layout); add bias, round, store.
-    auto epilogue = [&](const TcUnit &u, int buf) {
-        const int ow = u.ot * kTcMT + 16 * warp + lane;
-        const bool px_ok = lane < 16 && ow < p.OW;
-        const int co0 = u.c * g.NN;
-        float bias[4][8];
-#pragma unroll
-        for (int nb = 0; nb < 4; ++nb)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                bias[nb][e] = (p.has_bias && nb * 8 < g.NN)
-                                  ? load_f32(b + (int64_t)(co0 + nb * 8 + e) * p.bs) : 0.f;
-        for (int rr = 0; rr < g.R; ++rr) {
-            const int oh = u.ob * g.R + rr;
-            if (oh >= p.OH) break;
-            uint32_t v[4][8];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) +
-                                   (uint32_t)((buf * g.R + rr) * g.NN);
-#pragma unroll
-            for (int nb = 0; nb < 4; ++nb)
-                if (nb * 8 < g.NN) tc_ld8(taddr + (uint32_t)(nb * 8), v[nb]);
-            tc_wait_ld();
-            if (!px_ok) continue;
-            T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)oh * p.ys[2] + (int64_t)ow * p.ys[3] +
-                    (int64_t)co0 * p.ys[1];
-#pragma unroll
-            for (int nb = 0; nb < 4; ++nb) {
-                if (nb * 8 >= g.NN) break;
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    f[e] = bad ? __int_as_float(0x7fc00000) : __uint_as_float(v[nb][e]) + bias[nb][e];
-                if (g.vec_store) {
-                    uint4 o;
-                    o.x = pack2(f[0], f[1], (T *)nullptr);
-                    o.y = pack2(f[2], f[3], (T *)nullptr);
-                    o.z = pack2(f[4], f[5], (T *)nullptr);
-                    o.w = pack2(f[6], f[7], (T *)nullptr);
-                    *reinterpret_cast<uint4 *>(yp + nb * 8) = o;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) yp[(int64_t)(nb * 8 + e) * p.ys[1]] = from_f32<T>(f[e]);
+        __syncwarp();
+    } else {
+        // ------------- staging and TMEM drain (warps 0-3) -------------
+        auto stage_a = [&](const TcUnit &u, int buf) {
+            const uint32_t dst0 = sbase + (uint32_t)g.a_off[buf];
+            const int ih0 = u.ob * g.R * p.sh - p.pbh;
+            const int iw0 = u.ot * kTcMT * SW - p.pbw;
+            const T *xc = x + (int64_t)u.n * p.xs[0] + (int64_t)(8 * u.c) * p.xs[1];
+            for (int rp = warp; rp < g.rows_in * SW; rp += kTcProducers / 32) {
+                const int r = rp / SW, ph = rp - r * SW;
+                const int ih = ih0 + r;
+                const bool row_ok = ih >= 0 && ih < p.H;
+                const T *xrow = xc + (int64_t)(row_ok ? ih : 0) * p.xs[2];
+                for (int j = lane; j < g.NJ; j += 32) {
+                    const int iw = iw0 + j * SW + ph;
+                    const bool ok = row_ok && iw >= 0 && iw < p.W;
+                    tc_cp16(dst0 + (uint32_t)((rp * g.NJ + j) * 16),
+                            ok ? (const void *)(xrow + (int64_t)iw * p.xs[3]) : (const void *)x,
+                            ok ? 16 : 0);
                 }
             }
-        }
-    };
+            asm volatile("cp.async.commit_group;\n" ::: "memory");
+        };
+        // Chunk c's weights: row n (output channel c*NN + n), K slice q =
+        // 2*mma + half holds the 8 chunk channels of that tap as one
+        // 16-byte vector; channels outside n's group (and a missing second
+        // tap) are zero.  Each thread builds whole slices, QB at a time with
+        // every load in flight before the stores.
+        auto stage_b = [&](int c) {
+            constexpr int QB = 4;
+            const int nq = 2 * g.nmma;
+            const int total = g.NN * nq;
+            for (int e0 = t; e0 < total; e0 += QB * kTcProducers) {
+                union { uint4 u; T e[8]; } v[QB];
+                int dst[QB];
+#pragma unroll
+                for (int j = 0; j < QB; ++j) {
+                    v[j].u = make_uint4(0u, 0u, 0u, 0u);
+                    const int e = e0 + j * kTcProducers;
+                    dst[j] = -1;
+                    if (e < total) {
+                        const int n = e / nq, q = e - n * nq;
+                        const int tp = g.tap[q >> 1];
+                        const int kh = tp & 15;
+                        const int kw = (q & 1) ? ((tp >> 16) & 15) : ((tp >> 12) & 15);
+                        const int co = c * g.NN + n;
+                        const int cb = (n / p.Cout_g) * p.Cin_g;   // n's group's first chunk channel
+                        if (kw < p.KW) {
+                            const T *src = w + (int64_t)co * p.ws[0] + (int64_t)kh * p.ws[2] +
+                                           (int64_t)kw * p.ws[3];
+                            T vals[8];
+#pragma unroll
+                            for (int ci = 0; ci < 8; ++ci)
+                                vals[ci] = ci < p.Cin_g ? src[(int64_t)ci * p.ws[1]] : from_f32<T>(0.f);
+                            // the group sits at chunk channels cb .. cb + Cin_g - 1 (cb is 0 or 4)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                v[j].e[i] = cb == 0 ? vals[i] : (i >= 4 ? vals[i - 4] : from_f32<T>(0.f));
+                        }
+                        dst[j] = ((n >> 3) * g.b_sbo + q * 128 + (n & 7) * 16) / 16;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < QB; ++j)
+                    if (dst[j] >= 0) reinterpret_cast<uint4 *>(bsm)[dst[j]] = v[j].u;
+            }
+        };
+        // Stage unit u (buffer buf): its rows, and the chunk's weights when
+        // the chunk changes; then make the writes visible to the tensor
+        // core and arrive on full[buf].
+        auto stage = [&](const TcUnit &u, int buf, bool new_chunk) {
+            stage_a(u, buf);
+            if (new_chunk) stage_b(u.c);
+            if (t < g.NN)
+                bias_s[buf * 32 + t] = p.has_bias ? load_f32(b + (int64_t)(u.c * g.NN + t) * p.bs) : 0.f;
+            asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            tc_arrive(bar_full + 8u * buf);
+        };
+        // Drain unit u from TMEM block buf: warp w holds tile rows
+        // 16w..16w+15 in lanes 0-15 of its sub-partition (the M = 64
+        // layout); add the bias in fp32, round once, store 16-byte vectors.
+        auto epilogue = [&](const TcUnit &u, int buf) {
+            const int ow = u.ot * kTcMT + 16 * warp + lane;
+            const bool px_ok = lane < 16 && ow < p.OW;
+            const int co0 = u.c * g.NN;
+            const bool bad = *failed != 0;
+            for (int rr = 0; rr < g.R; ++rr) {
+                const int oh = u.ob * g.R + rr;
+                if (oh >= p.OH) break;
+                uint32_t v[4][8];
+                const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) +
+                                       (uint32_t)((buf * g.R + rr) * g.NN);
+#pragma unroll
+                for (int nb = 0; nb < 4; ++nb)
+                    if (nb * 8 < g.NN) tc_ld8(taddr + (uint32_t)(nb * 8), v[nb]);
+                tc_wait_ld();
+                if (!px_ok) continue;
+                T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)oh * p.ys[2] +
+                        (int64_t)ow * p.ys[3] + (int64_t)co0 * p.ys[1];
+#pragma unroll
+                for (int nb = 0; nb < 4; ++nb) {
+                    if (nb * 8 >= g.NN) break;
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        f[e] = bad ? __int_as_float(0x7fc00000)
+                                   : __uint_as_float(v[nb][e]) + bias_s[buf * 32 + nb * 8 + e];
+                    if (g.vec_store) {
+                        uint4 o;
+                        o.x = pack2(f[0], f[1], (T *)nullptr);
+                        o.y = pack2(f[2], f[3], (T *)nullptr);
+                        o.z = pack2(f[4], f[5], (T *)nullptr);
+                        o.w = pack2(f[6], f[7], (T *)nullptr);
+                        *reinterpret_cast<uint4 *>(yp + nb * 8) = o;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            yp[(int64_t)(nb * 8 + e) * p.ys[1]] = from_f32<T>(f[e]);
+                    }
+                }
+            }
+        };
 
-    TcUnit cur, prev;
-    cur.set(u0, g, p.N);
-    prev = cur;
-    TcUnit nxt = cur;
-    nxt.next(g, p.N);
-    stage_a(cur, 0);
-    int staged_c = -1;
-    for (int k = 0; k < nunits; ++k) {
-        const int buf = k & 1;
-        if (k > 0) {
-            // unit k-1's MMAs are done: its A buffer and TMEM block are free to read / refill
-            if (!mbar_wait(bars + 8u * (uint32_t)(buf ^ 1), (uint32_t)(((k - 1) >> 1) & 1))) bad = true;
-            tc_fence_after();
-        }
-        if (k + 1 < nunits) stage_a(nxt, buf ^ 1);
-        else asm volatile("cp.async.commit_group;\n" ::: "memory");
-        if (k > 0) epilogue(prev, buf ^ 1);
-        if (cur.c != staged_c) {   // every earlier MMA has completed
-            staged_c = cur.c;
-            stage_b(staged_c);
-        }
-        asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // unit k's rows have landed
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        if (t == 0) {
-            tc_fence_after();
-            issue(buf);
-        }
-        prev = cur;
-        cur = nxt;
+        TcUnit cur;
+        cur.set(u0, g, p.N);
+        TcUnit nxt = cur;
         nxt.next(g, p.N);
+        stage(cur, 0, true);
+        for (int k = 0; k < nunits; ++k) {
+            const int buf = k & 1;
+            // Every producer is done with unit k-1 (its bias slot and A
+            // buffer are free to refill).
+            tc_producer_sync();
+            if (k + 1 < nunits) {
+                const bool new_chunk = nxt.c != cur.c;
+                // New weights may be written only once unit k's MMAs (the
+                // last that read the old ones) have completed.
+                if (new_chunk) tc_wait(bar_done + 8u * buf, (uint32_t)((k >> 1) & 1), failed);
+                // A buffer buf^1 was last read by unit k-1's MMAs, whose
+                // completion this thread saw before draining them.
+                stage(nxt, buf ^ 1, new_chunk);
+            }
+            tc_wait(bar_done + 8u * buf, (uint32_t)((k >> 1) & 1), failed);
+            tc_fence_after();
+            epilogue(cur, buf);
+            tc_fence_before();
+            tc_arrive(bar_empty + 8u * buf);
+            cur = nxt;
+            nxt.next(g, p.N);
+        }
     }
-    const int klast = nunits - 1;
-    const uint32_t last_par = (uint32_t)((klast >> 1) & 1);
-    if (!mbar_wait(bars + 8u * (uint32_t)(klast & 1), last_par)) {
-        bad = true;
-        (void)mbar_wait(bars + 8u * (uint32_t)(klast & 1), last_par);   // once more before freeing TMEM
-    }
-    tc_fence_after();
-    epilogue(prev, klast & 1);
+    // Every MMA has completed (each unit's completion was waited for above)
+    // unless a wait gave up: then wait for the last unit's commit once more
+    // before the tensor memory is released.
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tc_dealloc(tmem, g.tmem_cols);
+    if (warp == 4) {
+        if (*failed) {
+            const int kl = nunits - 1;
+            uint32_t done = 0;
+            for (uint32_t i = 0; i < kTcSpinLimit && !done; ++i)
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                    "selp.u32 %0, 1, 0, p;\n\t}"
+                    : "=r"(done)
+                    : "r"(bar_done + 8u * (uint32_t)(kl & 1)), "r"((uint32_t)((kl >> 1) & 1))
+                    : "memory");
+        }
+        tc_dealloc(tmem, g.tmem_cols);
+    }
 }
 
 bool tc_supports(const gconv_desc &d, const Ptrs &q) {
