@@ -277,6 +277,11 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
         // ---------------- MMA issuer (one thread) ----------------
         if (lane == 0) {
             const uint64_t bdesc0 = tc_desc(sbase + (uint32_t)g.b_off, 128, (uint32_t)g.b_sbo);
+            // Per-MMA A start offsets in registers: the issue loop below is
+            // fully unrolled, so every descriptor is one add away.
+            int aoff[kTcMaxMMA];
+#pragma unroll
+            for (int i = 0; i < kTcMaxMMA; ++i) aoff[i] = atab[i];
             for (int k = 0; k < nunits; ++k) {
                 const int buf = k & 1;
                 tc_wait(bar_full + 8u * buf, (uint32_t)((k >> 1) & 1), failed);
@@ -285,17 +290,11 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
                 const uint64_t adesc0 = tc_desc(sbase + (uint32_t)g.a_off[buf], 16, 128);
                 for (int rr = 0; rr < g.R; ++rr) {
                     const uint32_t d = tmem + (uint32_t)((buf * g.R + rr) * g.NN);
-                    const int rowoff = rr * p.sh * SW * g.NJ;   // 16-byte units
-                    for (int i0 = 0; i0 < g.nmma; i0 += 8) {
-                        int a[8];
+                    const uint64_t arow = adesc0 + (uint64_t)(rr * p.sh * SW * g.NJ);   // 16-byte units
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) a[j] = atab[i0 + j];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (i0 + j < g.nmma)
-                                tc_mma(d, adesc0 + (uint64_t)(rowoff + a[j]),
-                                       bdesc0 + (uint64_t)(16 * (i0 + j)), g.idesc, i0 + j);
-                    }
+                    for (int i = 0; i < kTcMaxMMA; ++i)
+                        if (i < g.nmma)
+                            tc_mma(d, arow + (uint64_t)aoff[i], bdesc0 + (uint64_t)(16 * i), g.idesc, i);
                 }
                 tc_commit(bar_done + 8u * buf);
             }
