@@ -10,6 +10,7 @@
 
 #include "device_common.cuh"
 #include "gconv_internal.h"
+#include "launch.cuh"
 
 namespace gconv {
 namespace {
@@ -18,6 +19,10 @@ template <typename T, typename I>
 __global__ void __launch_bounds__(256)
 flat_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
             T *__restrict__ y, Params p, int64_t total) {
+    // Let the next kernel in the stream start launching; wait for the
+    // previous kernel's memory before reading global memory.
+    pdl_launch_dependents();
+    pdl_wait();
     const I OW = p.OW, OH = p.OH, Co = p.C_out;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -70,13 +75,16 @@ cudaError_t flat_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *lau
         const T *w = static_cast<const T *>(q.w);
         const T *b = static_cast<const T *>(q.b);
         T *y = static_cast<T *>(q.y);
+        cudaError_t e;
         if (total <= INT32_MAX)
-            flat_kernel<T, int><<<(unsigned)blocks, threads, 0, s>>>(x, w, b, y, p, total);
+            e = launch_pdl(flat_kernel<T, int>, dim3((unsigned)blocks), dim3(threads), 0, s, x, w,
+                           b, y, p, total);
         else
-            flat_kernel<T, int64_t><<<(unsigned)blocks, threads, 0, s>>>(x, w, b, y, p, total);
+            e = launch_pdl(flat_kernel<T, int64_t>, dim3((unsigned)blocks), dim3(threads), 0, s,
+                           x, w, b, y, p, total);
         (void)per_image;
         *launches = 1;
-        return cudaGetLastError();
+        return e != cudaSuccess ? e : cudaGetLastError();
     });
 }
 

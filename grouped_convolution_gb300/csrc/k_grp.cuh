@@ -26,6 +26,7 @@
 
 #include "device_common.cuh"
 #include "gconv_internal.h"
+#include "launch.cuh"
 
 namespace gconv {
 
@@ -89,6 +90,10 @@ template <typename T, int CIP, int MB, int SW>
 __global__ void __launch_bounds__(kGrpThreads, 2)
 grp_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
            T *__restrict__ y, Params p, GrpGeom g) {
+    // Let the next kernel in the stream start launching; wait for the
+    // previous kernel's memory before reading global memory.
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int P = grp_p(CIP);
     constexpr int PB = CIP * (int)sizeof(T);              // bytes per staged pixel
     constexpr int WPX = (P - 1) * SW + kGrpMaxKW;         // window pixels incl. unused taps

@@ -30,6 +30,7 @@
 
 #include "device_common.cuh"
 #include "gconv_internal.h"
+#include "launch.cuh"
 #include "tma.cuh"
 
 namespace gconv {
@@ -271,6 +272,10 @@ __global__ void __launch_bounds__(kMultThreads, kMultCtasPerSM)
 mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             const T *__restrict__ w, const T *__restrict__ b, T *__restrict__ y, Params p,
             MultGeom g) {
+    // Let the next kernel in the stream start launching; wait for the
+    // previous kernel's memory before reading global memory.
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int S = 16 / (int)sizeof(T);            // output pixels per thread
     extern __shared__ __align__(128) unsigned char mult_smem[];
     const uint32_t ring = smem_addr(mult_smem);       // raw stage s at ring + s*stage
@@ -419,10 +424,10 @@ cudaError_t mult_launch_t(const CUtensorMap &map, const Params &p, const Ptrs &q
     cudaError_t e = cudaFuncSetAttribute(mult_kernel<T, SW, MB, KWT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
-    mult_kernel<T, SW, MB, KWT><<<g.ctas, kMultThreads, g.smem, s>>>(
-        map, static_cast<const T *>(q.x), static_cast<const T *>(q.w),
-        static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
-    return cudaGetLastError();
+    e = launch_pdl(mult_kernel<T, SW, MB, KWT>, dim3(g.ctas), dim3(kMultThreads), g.smem, s, map,
+                   static_cast<const T *>(q.x), static_cast<const T *>(q.w),
+                   static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, int MB>

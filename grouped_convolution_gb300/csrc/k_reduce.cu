@@ -12,6 +12,7 @@
 // each thread its own (a small image or channel count with a big kernel).
 #include "device_common.cuh"
 #include "gconv_internal.h"
+#include "launch.cuh"
 
 namespace gconv {
 namespace {
@@ -22,6 +23,10 @@ template <typename T, int L>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
               T *__restrict__ y, Params p, int64_t total) {
+    // Let the next kernel in the stream start launching; wait for the
+    // previous kernel's memory before reading global memory.
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x % L;
     const int64_t per_block = kReduceThreads / L;
     const int taps = p.Cin_g * p.KH * p.KW;
@@ -83,11 +88,14 @@ cudaError_t reduce_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *l
         const T *w = static_cast<const T *>(q.w);
         const T *b = static_cast<const T *>(q.b);
         T *y = static_cast<T *>(q.y);
+        cudaError_t e;
         if (wide)
-            reduce_kernel<T, 32><<<(unsigned)blocks, kReduceThreads, 0, s>>>(x, w, b, y, p, total);
+            e = launch_pdl(reduce_kernel<T, 32>, dim3((unsigned)blocks), dim3(kReduceThreads), 0, s,
+                           x, w, b, y, p, total);
         else
-            reduce_kernel<T, 8><<<(unsigned)blocks, kReduceThreads, 0, s>>>(x, w, b, y, p, total);
-        return cudaGetLastError();
+            e = launch_pdl(reduce_kernel<T, 8>, dim3((unsigned)blocks), dim3(kReduceThreads), 0, s,
+                           x, w, b, y, p, total);
+        return e != cudaSuccess ? e : cudaGetLastError();
     });
 }
 

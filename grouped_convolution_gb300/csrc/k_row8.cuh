@@ -34,6 +34,7 @@
 #pragma once
 
 #include "gconv_internal.h"
+#include "launch.cuh"
 #include "stencil_math.cuh"
 #include "tma.cuh"
 
@@ -126,6 +127,10 @@ __global__ void __launch_bounds__(row8_max_threads(K), row8_ctas_per_sm(K))
 row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             const T *__restrict__ w, const T *__restrict__ b, T *__restrict__ y, Params p,
             Row8Geom g) {
+    // Let the next kernel in the stream start launching; wait for the
+    // previous kernel's memory before reading global memory.
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int SW = SH;                       // square strides only
     constexpr int VEC = row8_vec<T>(K);
     constexpr int P = VEC / 2;                   // channel pairs per thread
@@ -414,10 +419,10 @@ cudaError_t row8_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(row8_kernel<T, K, SH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    row8_kernel<T, K, SH><<<g.ctas, g.CVc * g.PG, smem, s>>>(
-        map, static_cast<const T *>(q.x), static_cast<const T *>(q.w),
-        static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
-    return cudaGetLastError();
+    e = launch_pdl(row8_kernel<T, K, SH>, dim3(g.ctas), dim3(g.CVc * g.PG), smem, s, map,
+                   static_cast<const T *>(q.x), static_cast<const T *>(q.w),
+                   static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T>

@@ -39,6 +39,7 @@
 
 #include "device_common.cuh"
 #include "gconv_internal.h"
+#include "launch.cuh"
 #include "tma.cuh"
 
 namespace gconv {
@@ -234,6 +235,10 @@ template <typename T, int SW>
 __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSM)
 tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
           T *__restrict__ y, Params p, TcGeom g) {
+    // Let the next kernel in the stream start launching; wait for the
+    // previous kernel's memory before reading global memory.
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(1024) unsigned char tc_smem[];
     const uint32_t sbase = smem_addr(tc_smem);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -498,10 +503,10 @@ cudaError_t tc_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const Tc
     cudaError_t e = cudaFuncSetAttribute(tc_kernel<T, SW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    tc_kernel<T, SW><<<g.ctas, kTcThreads, smem, s>>>(
-        static_cast<const T *>(q.x), static_cast<const T *>(q.w), static_cast<const T *>(q.b),
-        static_cast<T *>(q.y), p, g);
-    return cudaGetLastError();
+    e = launch_pdl(tc_kernel<T, SW>, dim3(g.ctas), dim3(kTcThreads), smem, s,
+                   static_cast<const T *>(q.x), static_cast<const T *>(q.w),
+                   static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t tc_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *launches) {

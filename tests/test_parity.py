@@ -341,6 +341,46 @@ def test_output_guard_bands_untouched(schedule):
     check(wl, x, w, b, y)
 
 
+CHAIN = [
+    # (name, schedule, layout cl, dtype, Cin_g, Cout_g, G, H, W, K, stride)
+    ("row8", "dw_row8", True, "bf16", 1, 1, 64, 30, 30, 3, 1),
+    ("mult", "dw_mult", False, "f16", 1, 1, 32, 40, 48, 5, 1),
+    ("tc", "grp_tc", True, "bf16", 4, 4, 16, 24, 70, 3, 1),
+    ("plane", "grp_plane", True, "f32", 4, 4, 8, 20, 20, 3, 1),
+    ("flat", "dw_flat", False, "f32", 1, 1, 16, 12, 12, 3, 1),
+]
+
+
+@pytest.mark.parametrize("case", CHAIN, ids=[c[0] for c in CHAIN])
+def test_chained_launches_see_previous_output(case):
+    """Kernels start early behind the previous launch (programmatic
+    dependent launch) but must read its finished output: y2 = conv(conv(x))
+    issued back to back many times on one stream, each y2 checked against
+    the oracle applied to the y1 the GPU produced."""
+    name, sched, cl, dtype, cig, cog, G, H, W, K, s = case
+    C = cig * G
+    wl = ConvWorkload(name, 91, N=2, C_in=C, H=H, W=W, C_out=C, groups=G, KH=K, KW=K,
+                      stride=(s, s), pad_before=(K // 2, K // 2), pad_after=(K // 2, K // 2),
+                      dtype=dtype, channels_last=cl, bias=True)
+    if cig * G != cog * G:
+        pytest.skip("chain needs C_out == C_in")
+    x, w, b = make_inputs(wl)
+    dev = torch.device("cuda")
+    xd, wd, bd = x.to(dev), w.to(dev), b.to(dev)
+    pad = K // 2
+    outs = []
+    for it in range(12):
+        y1 = gc.conv2d(xd, wd, bd, s, pad, pad, G, schedule=sched)
+        y2 = gc.conv2d(y1, wd, bd, s, pad, pad, G, schedule=sched)
+        outs.append((y1, y2))
+        xd = y2.clone() if it % 3 == 2 else xd   # feed results forward sometimes
+    torch.cuda.synchronize()
+    for y1, y2 in outs[-3:]:
+        ref, bound = oracle.conv2d(y1.cpu(), w, b, (s, s), (pad, pad), (pad, pad), G)
+        bad = oracle.violations(y2.cpu(), ref, bound, dtype)
+        assert not bad.any(), f"{int(bad.sum())} outputs differ from the oracle on the GPU's y1"
+
+
 def test_stream_argument_is_used():
     wl = workload(("st", 1, 1, 1, 16, 9, 9, 3, 3, (1, 1), (1, 1), (1, 1)), "f32", True, True, 29)
     x, w, b = make_inputs(wl)
