@@ -119,7 +119,7 @@ bool tc_geometry(const Params &p, TcGeom &g) {
     g.a_off[1] = (g.stage_bytes + 1023) / 1024 * 1024;
     g.b_off = g.a_off[1] + (g.stage_bytes + 1023) / 1024 * 1024;
     g.tab_off = g.b_off + (b_bytes + 127) / 128 * 128;
-    g.bias_off = g.tab_off + kTcMaxMMA * 4;
+    g.bias_off = g.tab_off + 2 * 4 * kTcMaxMMA * 16;   // descriptor table [buf][rr][mma]
     g.bar_off = g.bias_off + 2 * 32 * 4;
     g.smem = g.bar_off + 64;   // six mbarriers, TMEM address slot, failure flag
     if (g.smem > kTcSmemCap) return false;
@@ -247,7 +247,9 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
     const int nunits = per + ((int)blockIdx.x < extra ? 1 : 0);
     if (nunits <= 0) return;   // the same for the whole CTA
 
-    int *atab = reinterpret_cast<int *>(tc_smem + g.tab_off);   // A offsets, 16-byte units
+    // Complete (A, B) descriptor pairs of every MMA of a unit, per buffer and
+    // output row: [buf][rr][mma] as {A lo, A hi, B lo, B hi}.
+    uint4 *dtab = reinterpret_cast<uint4 *>(tc_smem + g.tab_off);
     float *bias_s = reinterpret_cast<float *>(tc_smem + g.bias_off);   // [2][32]
     // mbarriers: full[2] (rows + weights staged, 128 arrivals), done[2]
     // (the unit's MMAs completed, tcgen05.commit), empty[2] (TMEM block
@@ -269,9 +271,14 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
         *failed = 0;
         fence_barrier_init();
     }
-    for (int i = t; i < kTcMaxMMA; i += kTcThreads) {
+    for (int idx = t; idx < 2 * 4 * kTcMaxMMA; idx += kTcThreads) {
+        const int i = idx % kTcMaxMMA, rr = (idx / kTcMaxMMA) % 4, buf = idx / (4 * kTcMaxMMA);
         const int e = i < g.nmma ? g.tap[i] : g.tap[0];   // padded entries are never issued
-        atab[i] = (((e & 15) * SW + ((e >> 4) & 15)) * g.NJ + ((e >> 8) & 15));
+        const int off = (rr * p.sh * SW + (e & 15) * SW + ((e >> 4) & 15)) * g.NJ + ((e >> 8) & 15);
+        const uint64_t a = tc_desc(sbase + (uint32_t)g.a_off[buf] + (uint32_t)(16 * off), 16, 128);
+        const uint64_t bd = tc_desc(sbase + (uint32_t)g.b_off + (uint32_t)(256 * i), 128,
+                                    (uint32_t)g.b_sbo);
+        dtab[idx] = make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)bd, (uint32_t)(bd >> 32));
     }
     tc_fence_before();
     __syncthreads();
@@ -281,25 +288,24 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
     if (warp == 4) {
         // ---------------- MMA issuer (one thread) ----------------
         if (lane == 0) {
-            const uint64_t bdesc0 = tc_desc(sbase + (uint32_t)g.b_off, 128, (uint32_t)g.b_sbo);
-            // Per-MMA A start offsets in registers: the issue loop below is
-            // fully unrolled, so every descriptor is one add away.
-            int aoff[kTcMaxMMA];
-#pragma unroll
-            for (int i = 0; i < kTcMaxMMA; ++i) aoff[i] = atab[i];
             for (int k = 0; k < nunits; ++k) {
                 const int buf = k & 1;
                 tc_wait(bar_full + 8u * buf, (uint32_t)((k >> 1) & 1), failed);
                 if (k >= 2) tc_wait(bar_empty + 8u * buf, (uint32_t)(((k - 2) >> 1) & 1), failed);
                 tc_fence_after();
-                const uint64_t adesc0 = tc_desc(sbase + (uint32_t)g.a_off[buf], 16, 128);
                 for (int rr = 0; rr < g.R; ++rr) {
                     const uint32_t d = tmem + (uint32_t)((buf * g.R + rr) * g.NN);
-                    const uint64_t arow = adesc0 + (uint64_t)(rr * p.sh * SW * g.NJ);   // 16-byte units
+                    const uint4 *row = dtab + (buf * 4 + rr) * kTcMaxMMA;
+                    for (int i0 = 0; i0 < g.nmma; i0 += 8) {
+                        uint4 v[8];
 #pragma unroll
-                    for (int i = 0; i < kTcMaxMMA; ++i)
-                        if (i < g.nmma)
-                            tc_mma(d, arow + (uint64_t)aoff[i], bdesc0 + (uint64_t)(16 * i), g.idesc, i);
+                        for (int j = 0; j < 8; ++j) v[j] = row[i0 + j];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (i0 + j < g.nmma)
+                                tc_mma(d, ((uint64_t)v[j].y << 32) | v[j].x,
+                                       ((uint64_t)v[j].w << 32) | v[j].z, g.idesc, i0 + j);
+                    }
                 }
                 tc_commit(bar_done + 8u * buf);
             }
