@@ -154,10 +154,11 @@ def test_dw_mult_geometry_matches_oracle(case, dtype):
     check(wl, x, w, b, y)
 
 
-# grp_tc (tensor-core implicit GEMM) tile geometry: several 64-pixel column
+# grp_tc (tensor-core schedule) tile geometry: several 128-pixel column
 # tiles and a ragged last tile, row blocks shorter than a unit, 4 and 8
 # input channels per group, 8 / 16 / 32 output channels per 8-channel
-# chunk, strides 1 to 3, kernels from 1x1 to 9x9, asymmetric padding.
+# chunk, strides 1 to 3, kernels from 1x1 to 9x9, asymmetric padding, and
+# more staged units than CTAs.
 TC_CASES = [
     # name, N, Cin_g, Cout_g, G, H, W, KH, KW, stride, pad_before, pad_after
     ("c5_small", 1, 4, 8, 4, 33, 40, 9, 9, (2, 2), (4, 4), (4, 4)),
@@ -166,6 +167,10 @@ TC_CASES = [
     ("cout16_s3", 1, 4, 16, 2, 10, 66, 3, 5, (3, 1), (0, 2), (1, 2)),
     ("k1", 1, 8, 16, 1, 5, 9, 1, 1, (1, 1), (0, 0), (0, 0)),
     ("k9x7_ragged", 1, 4, 8, 2, 20, 129, 9, 7, (2, 2), (4, 3), (4, 3)),
+    # several staged units per CTA (more units than CTAs): accumulator
+    # blocks reused, weights restaged when a CTA's units change chunk
+    ("many_units", 2, 4, 8, 64, 64, 64, 9, 9, (2, 2), (4, 4), (4, 4)),
+    ("many_units_2tiles", 2, 8, 16, 32, 24, 160, 3, 3, (1, 1), (1, 1), (1, 1)),
 ]
 
 
