@@ -178,12 +178,13 @@ class ClockSampler:
 # Source files that define each schedule's kernel; the recorded DRAM traffic
 # of a kernel is void once any of them changes.
 KERNEL_SOURCES = {
-    "dw_row8": ["k_row8.cuh", "k_row8.cu", "stencil_math.cuh", "device_common.cuh", "tma.cuh"],
-    "dw_flat": ["k_flat.cu", "device_common.cuh"],
-    "dw_mult": ["k_mult.cuh", "k_mult.cu", "device_common.cuh", "tma.cuh"],
-    "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh"],
-    "grp_reduce": ["k_reduce.cu", "device_common.cuh"],
-    "grp_tc": ["k_tc.cu", "device_common.cuh", "tma.cuh"],
+    "dw_row8": ["k_row8.cuh", "k_row8.cu", "stencil_math.cuh", "device_common.cuh", "tma.cuh",
+                "launch.cuh"],
+    "dw_flat": ["k_flat.cu", "device_common.cuh", "launch.cuh"],
+    "dw_mult": ["k_mult.cuh", "k_mult.cu", "device_common.cuh", "tma.cuh", "launch.cuh"],
+    "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh", "launch.cuh"],
+    "grp_reduce": ["k_reduce.cu", "device_common.cuh", "launch.cuh"],
+    "grp_tc": ["k_tc.cu", "device_common.cuh", "tma.cuh", "launch.cuh"],
 }
 
 
@@ -208,7 +209,7 @@ def recorded_traffic(schedule, workload):
             table = json.load(f)
     except (OSError, ValueError):
         return None
-    ent = table.get(workload)
+    ent = table.get(f"{workload}@{schedule}") or table.get(workload)
     if not ent or ent.get("schedule") != schedule or \
             ent.get("source_sha") != kernel_source_sha(schedule):
         return None
@@ -220,7 +221,7 @@ def recorded_traffic(schedule, workload):
 class ConvCase:
     """One workload bound once, with R rotating input/output sets."""
 
-    def __init__(self, name, sets, device):
+    def __init__(self, name, sets, device, schedule=None):
         import torch
         import grouped_convolution_gb300 as gc
         from grouped_convolution_gb300.inputs import WORKLOADS, make_inputs
@@ -232,6 +233,8 @@ class ConvCase:
         self.b = b.to(device) if b is not None else None
         self.desc = gc.conv_bind(x, w, b, self.wl.stride, self.wl.pad_before,
                                  self.wl.pad_after, 1, self.wl.groups)
+        if schedule is not None:
+            self.desc.schedule = gc.SCHEDULES[schedule]
         xd = x.to(device)
         self.xs = [xd] + [xd.clone() for _ in range(sets - 1)]
         self.ys = [gc.empty_output(self.desc, xd) for _ in range(sets)]
@@ -427,25 +430,36 @@ def per_config(args, world, l2, hbm_peak, dev):
     from grouped_convolution_gb300.inputs import WORKLOADS
     out = {}
     steps = max(20, min(args.steps, 2000))
-    for name in WORKLOADS:
-        one = ConvCase(name, 1, dev)
+    def measure(name, schedule=None):
+        one = ConvCase(name, 1, dev, schedule)
         R = sets_needed(one.footprint(), l2)
         del one
         torch.cuda.empty_cache()
-        c = ConvCase(name, R, dev)
+        c = ConvCase(name, R, dev, schedule)
         ms, _ = time_graph([c], steps, max(3, min(args.warmup, 50)), world)
         t = ms / steps * 1e-3
         gbs = c.bytes / t / 1e9
         fma_peak = SMS * FMA_LANES * MAX_MHZ * 1e6
-        out[name] = {"schedule": c.schedule, "us": round(t * 1e6, 3),
-                     "GB_s": round(gbs, 1), "Gpix_s": round(c.pix / t / 1e9, 3),
-                     "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
-                     "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
-                     "TFMA_s": round(c.fma / t / 1e12, 3),
-                     "frac_of_fma_peak_2070mhz": round(c.fma / t / fma_peak, 4),
-                     "bytes": c.bytes, "fma": c.fma}
+        res = {"schedule": c.schedule, "us": round(t * 1e6, 3),
+               "GB_s": round(gbs, 1), "Gpix_s": round(c.pix / t / 1e9, 3),
+               "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+               "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+               "TFMA_s": round(c.fma / t / 1e12, 3),
+               "frac_of_fma_peak_2070mhz": round(c.fma / t / fma_peak, 4),
+               "bytes": c.bytes, "fma": c.fma}
         del c
         torch.cuda.empty_cache()
+        return res
+
+    for name in WORKLOADS:
+        out[name] = measure(name)
+        # A call the picker sends to the tensor cores is also timed on the
+        # direct stencil (no tensor cores) that would take it otherwise.
+        if out[name]["schedule"] == "grp_tc":
+            st = measure(name, "grp_plane")
+            out[name]["direct_stencil"] = {k: st[k] for k in (
+                "schedule", "us", "GB_s", "frac_of_measured_hbm", "TFMA_s",
+                "frac_of_fma_peak_2070mhz")}
     return out
 
 
