@@ -305,32 +305,46 @@ def time_graph(cases, steps, warmup, world, chunk=200):
     return max_over_ranks(ms, world), launches
 
 
-def time_e2e(cases, steps, world):
+def time_e2e(cases, steps, world, lanes=3):
     """Same metric through the public API with host buffers: every step copies
     its input from pinned host memory, runs the convolutions and reads the
-    results back to pinned host memory."""
+    results back to pinned host memory.  Steps rotate over `lanes` streams,
+    each with its own device and pinned output buffers, so step i's input
+    copy overlaps step i-1's kernels and step i-2's read-back (the copy
+    engines and the SMs work at once, as a streaming user would run them)."""
     import torch
+    gc = cases[0].gc
     host_x = cases[0].x_host.pin_memory()
-    dev_x = cases[0].xs[0]
-    outs = [torch.empty(c.ys[0].shape, dtype=c.ys[0].dtype).pin_memory() for c in cases]
+    streams = [torch.cuda.Stream() for _ in range(lanes)]
+    dev_x = [cases[0].xs[0]] + [cases[0].xs[0].clone() for _ in range(lanes - 1)]
+    dev_y = [[gc.empty_output(c.desc, dev_x[0]) for c in cases] for _ in range(lanes)]
+    outs = [[torch.empty(c.ys[0].shape, dtype=c.ys[0].dtype).pin_memory() for c in cases]
+            for _ in range(lanes)]
     h2d = host_x.numel() * host_x.element_size()
-    d2h = sum(o.numel() * o.element_size() for o in outs)
-    stream = torch.cuda.current_stream()
+    d2h = sum(o.numel() * o.element_size() for o in outs[0])
+    main = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(3):  # warm-up
-        dev_x.copy_(host_x, non_blocking=True)
-        for c, o in zip(cases, outs):
-            c.fwd(c.desc, dev_x, c.w, c.b, c.ys[0])
-            o.copy_(c.ys[0], non_blocking=True)
+
+    def step(i):
+        k = i % lanes
+        with torch.cuda.stream(streams[k]):
+            dev_x[k].copy_(host_x, non_blocking=True)
+            for c, y, o in zip(cases, dev_y[k], outs[k]):
+                c.fwd(c.desc, dev_x[k], c.w, c.b, y, streams[k])
+                o.copy_(y, non_blocking=True)
+
+    for i in range(3 * lanes):  # warm-up
+        step(i)
     torch.cuda.synchronize()
     barrier(world)
-    start.record(stream)
-    for _ in range(steps):
-        dev_x.copy_(host_x, non_blocking=True)
-        for c, o in zip(cases, outs):
-            c.fwd(c.desc, dev_x, c.w, c.b, c.ys[0])
-            o.copy_(c.ys[0], non_blocking=True)
-    end.record(stream)
+    start.record(main)
+    for st in streams:
+        st.wait_event(start)
+    for i in range(steps):
+        step(i)
+    for st in streams:
+        main.wait_stream(st)
+    end.record(main)
     torch.cuda.synchronize()
     barrier(world)
     return max_over_ranks(start.elapsed_time(end), world), h2d, d2h
