@@ -34,6 +34,14 @@
  * (no workspace), keeps no pointer after a call returns and never
  * synchronises; kernels run asynchronously on the caller's stream.
  *
+ * Ordering.  Each forward is one kernel launched with programmatic
+ * dependent launch: it may start while the previous kernel on the stream is
+ * finishing, but it waits for that kernel's memory before its first read of
+ * x, w or bias, so stream order is kept exactly (a forward may consume the
+ * previous kernel's output).  It also lets the next kernel on the stream
+ * start early; a next kernel that does not opt in to programmatic launch
+ * simply waits for it to complete, as usual.
+ *
  * Errors.  Every entry point returns a gconv_status; nothing throws or
  * aborts across the ABI.  conv_strerror() names a status.
  *
