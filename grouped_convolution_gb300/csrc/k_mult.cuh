@@ -297,7 +297,9 @@ mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     // rows from its first input row.
     auto box_x = [&](const MultItem &it) { return it.cc * g.OWc * p.sw - p.pbw - g.shift; };
     auto box_y = [&](const MultItem &it) { return it.bd * g.BR * p.sh - p.pbh; };
+    int issued = 0;   // boxes issued (thread 0)
     auto issue = [&](const MultItem &it, int s) {   // one thread
+        ++issued;
         const uint32_t bar = bars + 8u * s;
         mbar_arrive_expect_tx(bar, (uint32_t)g.box_bytes);
         tma_load_4d(ring + (uint32_t)(s * g.stage), &xmap, bar, box_x(it), box_y(it), it.c, it.n);
@@ -359,17 +361,22 @@ mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     const int nq = (kMultRT - 1) * p.sh + p.KH;       // band rows a thread reads
 
     int cur_c = -1;
-    int drain = 0;              // stages whose wait gave up
-    uint32_t drain_par[2] = {0u, 0u};
+    int waited = 0;   // boxes this thread has seen arrive (box k uses stage k & 1)
+    bool ok = true;   // every wait of this thread so far succeeded
     for (int it = i0, k = 0; it < i1; ++it, ++k) {
         const int s = k & 1;
         float *band = band0 + s * band_floats;
         if (g.use_tma) {
-            const uint32_t par = (uint32_t)((k >> 1) & 1);
-            if (!mbar_wait(bars + 8u * s, par)) {
-                *failed = 1;
-                drain |= 1 << s;
-                drain_par[s] = par;
+            // After this thread's first failed wait nothing more is waited
+            // for; the waits of the others give up once the CTA is marked
+            // failed, and thread 0 issues nothing after it.
+            if (ok) {
+                if (mbar_wait(bars + 8u * s, (uint32_t)((k >> 1) & 1), failed)) {
+                    ++waited;
+                } else {
+                    ok = false;
+                    *failed = 1;
+                }
             }
         } else {
             fill(item, s);
@@ -409,10 +416,13 @@ mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
         }
         item.next(g, p.N);
     }
-    // A box whose wait gave up may still land: wait for it once more
-    // (bounded) before the CTA's shared memory is released.
-    for (int st = 0; st < 2; ++st)
-        if (drain & (1 << st)) (void)mbar_wait(bars + 8u * st, drain_par[st]);
+    // After a failed wait, boxes issued but never seen to arrive may still be
+    // landing in this CTA's shared memory: wait for each once more (bounded)
+    // before the CTA exits.  Boxes k = 0 .. issued-1 went to stage k & 1.
+    if (t == 0 && g.use_tma && *failed) {
+        for (int q = waited; q < issued; ++q)
+            (void)mbar_wait(bars + 8u * (uint32_t)(q & 1), (uint32_t)((q >> 1) & 1));
+    }
 }
 
 // Host launcher for one dtype: geometry, tensor map (or plain fills),

@@ -28,9 +28,12 @@
 //    rounded once to the output dtype and stored with coalesced 4/8/16-byte
 //    stores through a pointer that advances one output row at a time.
 //  - A wait that gives up (it should never happen) poisons the waiting
-//    thread's accumulators and bias with NaN, so from then on its outputs
-//    are NaN: the failure is visible in the result instead of hanging the
-//    GPU, and the store path carries no per-value check.
+//    thread's accumulators and bias with NaN and marks the CTA failed: no
+//    box is issued or waited for after that, every thread poisons its own
+//    accumulators at its next stage, so the outputs are NaN (the failure is
+//    visible in the result instead of hanging the GPU, and the store path
+//    carries no per-value check); before exiting, the issuing thread waits
+//    once more (bounded) for every box it issued that was not seen to arrive.
 #pragma once
 
 #include "gconv_internal.h"
@@ -156,6 +159,9 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
 
     const uint32_t ring = smem_addr(row8_ring);
     const uint32_t bars = ring + (uint32_t)(g.NS * g.stage);   // NS mbarriers
+    // Set once any wait of the CTA gives up: no box is issued or waited for
+    // after it (the stores become NaN).
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(row8_ring + g.NS * g.stage + 8 * g.NS);
     // fp32 weights [tap][chunk channel] and bias, after the barriers
     float *wsm = reinterpret_cast<float *>(row8_ring + g.NS * g.stage + 8 * g.NS + 16);
     const int row_bytes = g.Win * g.pitch;       // one staged input row
@@ -164,9 +170,11 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     // holds U consecutive input rows of one run.
     Row8Run prun{};
     int pnext_u = 0, pst = 0, pnst = 0, pslot = 0;
+    int pissued = 0;       // boxes issued so far
     bool pdone = false;
     auto issue = [&]() {
         if (pdone) return;
+        ++pissued;
         const uint32_t bar = bars + 8u * pslot;
         mbar_arrive_expect_tx(bar, (uint32_t)g.box_bytes);
         tma_load_4d(ring + (uint32_t)(pslot * g.stage), &xmap, bar, prun.hc * g.CVc * VEC,
@@ -233,6 +241,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     if (t == 0) {
         tma_prefetch_map(&xmap);
         for (int i = 0; i < g.NS; ++i) mbar_init(bars + 8u * i, 1);
+        *abort_flag = 0;
         fence_barrier_init();
         prun = row8_run_at<K, SH>(o0, o1, p.OH, g.CC, g.HC);
         pnext_u = o0 + prun.rows;
@@ -246,6 +255,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     uint32_t cphase = 0;  // parity of that stage's current use
 
     bool bad = false;     // a box wait gave up (outputs become NaN)
+    int cwaited = 0;      // boxes this thread has seen arrive
     int u = o0;
     while (u < o1) {
         const Row8Run run = row8_run_at<K, SH>(u, o1, p.OH, g.CC, g.HC);
@@ -282,11 +292,18 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
         const uint32_t win0 = ring + (uint32_t)(cvl * VB + pg * S * SW * g.pitch);
 
         for (int r0 = 0; r0 < run.nin; r0 += U) {
-            if (!mbar_wait(bars + 8u * cslot, cphase)) {
-                // The box did not arrive: poison every open accumulator and
-                // the bias, so every output this thread stores from now on
-                // is NaN (the bias is poisoned again after a weight reload).
+            const bool arrived = !bad && mbar_wait(bars + 8u * cslot, cphase, abort_flag);
+            if (arrived) ++cwaited;
+            // Thread 0 reads the flag here, off the refill's critical path: a
+            // failure seen one stage late costs one more box, drained below.
+            if (t == 0 && *abort_flag) pdone = true;
+            if (!arrived && !bad) {
+                // The box did not arrive (or another thread's did not): poison
+                // every open accumulator and the bias, so every output this
+                // thread stores from now on is NaN (the bias is poisoned
+                // again after a weight reload), and stop the ring.
                 bad = true;
+                *abort_flag = 1;
 #pragma unroll
                 for (int s = 0; s < R; ++s)
 #pragma unroll
@@ -357,6 +374,12 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             if (t == 0) issue();      // refill it with the box NS stages ahead
         }
     }
+    // After a failed wait, boxes issued but never seen to arrive may still be
+    // landing in this CTA's shared memory: wait for each once more (bounded)
+    // before the CTA exits.  Issue and arrival follow the same slot order.
+    if (t == 0 && *abort_flag)
+        for (int q = cwaited; q < pissued; ++q)
+            (void)mbar_wait(bars + 8u * (uint32_t)(q % g.NS), (uint32_t)((q / g.NS) & 1));
 }
 
 // Launch geometry for one call; false when the shape does not fit.

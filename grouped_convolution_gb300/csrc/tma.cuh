@@ -21,7 +21,7 @@
 
 namespace gconv {
 
-constexpr uint32_t kTmaSpinLimit = 1u << 26;
+constexpr uint32_t kTmaSpinLimit = 1u << 22;
 
 // Encode a rank-4 tiled map over a tensor whose innermost dim is dims[0].
 // strides_bytes[i] is the byte stride of dims[i + 1].  Returns false when
@@ -58,8 +58,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // Poll the barrier until the phase with the given parity has completed.
-// Returns false if it did not complete within kTmaSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Returns false if it did not complete within kTmaSpinLimit polls, or, when
+// `abort` is given, as soon as *abort is set after the first 64 polls (the
+// flag is read only on that slow path).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const volatile int *abort = nullptr) {
     for (uint32_t i = 0; i < kTmaSpinLimit; ++i) {
         uint32_t done;
         asm volatile(
@@ -70,6 +73,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
+        if (abort && i >= 64 && *abort) return false;
     }
     return false;
 }
