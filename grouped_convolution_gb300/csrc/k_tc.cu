@@ -25,12 +25,12 @@
 //    one entry further on (leading byte offset 16).
 //  - B (the chunk's weights) is staged once per chunk in the canonical
 //    K-major layout, its K slices in the order the MMAs consume them.
-//  - A work unit is R output rows of one (image, ow tile, chunk); one
-//    thread issues its R x (taps / 2) MMAs into an R x NN block of TMEM
-//    columns and commits them to an mbarrier.  Units are double-buffered:
+//  - A work unit is R output rows of one (image, ow tile, chunk); R
+//    threads in separate warps each issue one row's taps / 2 MMAs into
+//    that row's NN TMEM columns and commit them to one mbarrier.  Units are double-buffered:
 //    while the tensor core works on unit k, the CTA stages unit k+1 and
 //    drains unit k-1 from TMEM (tcgen05.ld), adds the bias in fp32, rounds
-//    once and stores 16-byte vectors.  Two CTAs share an SM (two MMA
+//    once and stores 16-byte vectors.  Two CTAs share an SM (eight MMA
 //    issuers; an M = 64 MMA uses half of the tensor core's lanes).
 //  - Every mbarrier wait is bounded; a wait that gives up marks the CTA
 //    failed, its outputs are written as NaN and no TMEM is freed before the
@@ -46,7 +46,8 @@ namespace gconv {
 namespace {
 
 constexpr int kTcProducers = 128;   // warps 0-3: staging and TMEM drain
-constexpr int kTcThreads = 160;     // + warp 4: MMA issue
+constexpr int kTcIssuers = 4;       // warps 4-7: MMA issue, one output row each
+constexpr int kTcThreads = kTcProducers + 32 * kTcIssuers;
 constexpr int kTcMT = 64;          // output pixels per tile (MMA M)
 constexpr int kTcMaxMMA = 48;      // tap pairs per output row (9x9: 45)
 constexpr int kTcSmemCap = 112 * 1024;   // two CTAs per SM
@@ -252,8 +253,8 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
     uint4 *dtab = reinterpret_cast<uint4 *>(tc_smem + g.tab_off);
     float *bias_s = reinterpret_cast<float *>(tc_smem + g.bias_off);   // [2][32]
     // mbarriers: full[2] (rows + weights staged, 128 arrivals), done[2]
-    // (the unit's MMAs completed, tcgen05.commit), empty[2] (TMEM block
-    // drained, 128 arrivals).
+    // (the unit's MMAs completed: one tcgen05.commit per issuer), empty[2]
+    // (TMEM block drained, 128 arrivals).
     const uint32_t bar_full = sbase + (uint32_t)g.bar_off;
     const uint32_t bar_done = bar_full + 16u;
     const uint32_t bar_empty = bar_full + 32u;
@@ -265,7 +266,7 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
     if (t == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_full + 8u * i, kTcProducers);
-            mbar_init(bar_done + 8u * i, 1);
+            mbar_init(bar_done + 8u * i, kTcIssuers);
             mbar_init(bar_empty + 8u * i, kTcProducers);
         }
         *failed = 0;
@@ -285,15 +286,24 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == 4) {
-        // ---------------- MMA issuer (one thread) ----------------
+    if (warp >= 4) {
+        // ------- MMA issue: lane 0 of warp 4 + rr issues output row rr -------
+        // One thread issues a small MMA every ~30 ns at best, well below the
+        // tensor core's rate for these shapes; four issuers per CTA (eight
+        // per SM) bring the SM to ~12-14 ns per MMA.  An issuer without a
+        // row (R < 4) still arrives on done, so every unit's phase completes.
+        const int rr = warp - 4;
         if (lane == 0) {
             for (int k = 0; k < nunits; ++k) {
                 const int buf = k & 1;
                 tc_wait(bar_full + 8u * buf, (uint32_t)((k >> 1) & 1), failed);
                 if (k >= 2) tc_wait(bar_empty + 8u * buf, (uint32_t)(((k - 2) >> 1) & 1), failed);
                 tc_fence_after();
-                for (int rr = 0; rr < g.R; ++rr) {
+                if (rr >= g.R) {
+                    tc_arrive(bar_done + 8u * buf);
+                    continue;
+                }
+                {
                     const uint32_t d = tmem + (uint32_t)((buf * g.R + rr) * g.NN);
                     const uint4 *row = dtab + (buf * 4 + rr) * kTcMaxMMA;
                     for (int i0 = 0; i0 < g.nmma; i0 += 8) {
