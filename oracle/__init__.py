@@ -1,4 +1,6 @@
-"""CPU fp64 oracle for 2-D grouped / depthwise convolution.
+"""CPU fp64 oracle for grouped / depthwise convolution: forward (2-D and, as
+its H = 1 case, 1-D; any dilation), transposed, and the backward (gradients
+with respect to x, w and bias).
 
 TEST INFRASTRUCTURE, not part of the product path: only ``tests/``,
 ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
@@ -63,15 +65,24 @@ def _load():
             lib = ctypes.CDLL(build())
             i64, dp = ctypes.c_int64, ctypes.POINTER(ctypes.c_double)
             lib.oracle_out_size.restype = i64
-            lib.oracle_out_size.argtypes = [i64] * 5
+            lib.oracle_out_size.argtypes = [i64] * 6
+            lib.oracle_transposed_out_size.restype = i64
+            lib.oracle_transposed_out_size.argtypes = [i64] * 7
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
-            common = [dp, dp, dp] + [i64] * 14
+            common = [dp, dp, dp] + [i64] * 16
+            ip = ctypes.POINTER(ctypes.c_int64)
             lib.oracle_conv2d_f64.restype = ctypes.c_int
             lib.oracle_conv2d_f64.argtypes = common + [dp, dp]
             lib.oracle_conv2d_f64_points.restype = ctypes.c_int
-            lib.oracle_conv2d_f64_points.argtypes = (
-                common + [i64, ctypes.POINTER(ctypes.c_int64), dp, dp])
+            lib.oracle_conv2d_f64_points.argtypes = common + [i64, ip, dp, dp]
+            tcommon = [dp, dp, dp] + [i64] * 18
+            lib.oracle_conv_transpose2d_f64.restype = ctypes.c_int
+            lib.oracle_conv_transpose2d_f64.argtypes = tcommon + [dp, dp]
+            lib.oracle_conv_transpose2d_f64_points.restype = ctypes.c_int
+            lib.oracle_conv_transpose2d_f64_points.argtypes = tcommon + [i64, ip, dp, dp]
+            lib.oracle_conv2d_backward_f64.restype = ctypes.c_int
+            lib.oracle_conv2d_backward_f64.argtypes = common + [dp] * 6
             _lib = lib
     return _lib
 
@@ -98,9 +109,16 @@ def _pair(v):
     return v
 
 
-def out_size(in_size: int, k: int, s: int, pb: int, pa: int) -> int:
+def out_size(in_size: int, k: int, s: int, pb: int, pa: int, d: int = 1) -> int:
     """Output length along one spatial dim (-1 when the window never fits)."""
-    return int(_load().oracle_out_size(in_size, k, s, pb, pa))
+    return int(_load().oracle_out_size(in_size, k, s, pb, pa, d))
+
+
+def transposed_out_size(in_size: int, k: int, s: int, pb: int, pa: int, op: int = 0,
+                        d: int = 1) -> int:
+    """Output length of a transposed convolution along one dim (-1 when
+    nothing is left after the crop, or an argument is out of range)."""
+    return int(_load().oracle_transposed_out_size(in_size, k, s, pb, pa, op, d))
 
 
 def num_threads() -> int:
@@ -111,7 +129,7 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double)) if a is not None else None
 
 
-def _prep(x, w, b, stride, pad_before, pad_after, groups):
+def _prep(x, w, b, stride, pad_before, pad_after, groups, dilation=1):
     x = _as_f64(x)
     w = _as_f64(w)
     b = _as_f64(b)
@@ -128,18 +146,19 @@ def _prep(x, w, b, stride, pad_before, pad_after, groups):
         raise ValueError("C_in must equal Cin_g * groups")
     if b is not None and b.shape != (C_out,):
         raise ValueError("bias must be [C_out]")
-    OH = out_size(H, KH, sh, pbh, pah)
-    OW = out_size(W, KW, sw, pbw, paw)
+    dh, dw = _pair(dilation)
+    OH = out_size(H, KH, sh, pbh, pah, dh)
+    OW = out_size(W, KW, sw, pbw, paw, dw)
     if OH < 0 or OW < 0:
         raise ValueError("window larger than the padded input")
-    dims = (N, C_in, H, W, C_out, groups, KH, KW, sh, sw, pbh, pbw, pah, paw)
+    dims = (N, C_in, H, W, C_out, groups, KH, KW, sh, sw, pbh, pbw, pah, paw, dh, dw)
     return x, w, b, dims, (N, C_out, OH, OW)
 
 
-def conv2d(x, w, b=None, stride=1, pad_before=0, pad_after=None, groups=1):
+def conv2d(x, w, b=None, stride=1, pad_before=0, pad_after=None, groups=1, dilation=1):
     """Reference convolution.  Returns (y, bound) as float64 arrays of shape
     [N, C_out, OH, OW]."""
-    x, w, b, dims, oshape = _prep(x, w, b, stride, pad_before, pad_after, groups)
+    x, w, b, dims, oshape = _prep(x, w, b, stride, pad_before, pad_after, groups, dilation)
     y = np.empty(oshape, dtype=np.float64)
     bound = np.empty(oshape, dtype=np.float64)
     rc = _load().oracle_conv2d_f64(_ptr(x), _ptr(w), _ptr(b), *dims, _ptr(y), _ptr(bound))
@@ -148,10 +167,10 @@ def conv2d(x, w, b=None, stride=1, pad_before=0, pad_after=None, groups=1):
     return y, bound
 
 
-def conv2d_points(x, w, b, stride, pad_before, pad_after, groups, pts):
+def conv2d_points(x, w, b, stride, pad_before, pad_after, groups, pts, dilation=1):
     """Reference values at selected outputs.  ``pts`` is an [P, 4] integer
     array of (n, co, oh, ow).  Returns (y, bound), each of length P."""
-    x, w, b, dims, _ = _prep(x, w, b, stride, pad_before, pad_after, groups)
+    x, w, b, dims, _ = _prep(x, w, b, stride, pad_before, pad_after, groups, dilation)
     pts = np.ascontiguousarray(np.asarray(pts, dtype=np.int64).reshape(-1, 4))
     y = np.empty(len(pts), dtype=np.float64)
     bound = np.empty(len(pts), dtype=np.float64)
@@ -161,6 +180,136 @@ def conv2d_points(x, w, b, stride, pad_before, pad_after, groups, pts):
     if rc != 0:
         raise ValueError("oracle rejected the arguments or a point")
     return y, bound
+
+
+def _prep_transposed(x, w, b, stride, pad_before, pad_after, output_padding, groups,
+                     dilation):
+    x = _as_f64(x)
+    w = _as_f64(w)
+    b = _as_f64(b)
+    if x.ndim == 3:
+        x = x[None]
+    if x.ndim != 4 or w.ndim != 4:
+        raise ValueError("x must be [N,C,H,W] (or [C,H,W]); w must be [C_in,Cog,KH,KW]")
+    sh, sw = _pair(stride)
+    pbh, pbw = _pair(pad_before)
+    pah, paw = _pair(pad_before if pad_after is None else pad_after)
+    oph, opw = _pair(output_padding)
+    dh, dw = _pair(dilation)
+    N, C_in, H, W = x.shape
+    Cw, Cout_g, KH, KW = w.shape
+    if Cw != C_in or C_in % groups:
+        raise ValueError("w must be [C_in, C_out/groups, KH, KW]")
+    C_out = Cout_g * groups
+    if b is not None and b.shape != (C_out,):
+        raise ValueError("bias must be [C_out]")
+    OH = transposed_out_size(H, KH, sh, pbh, pah, oph, dh)
+    OW = transposed_out_size(W, KW, sw, pbw, paw, opw, dw)
+    if OH < 0 or OW < 0:
+        raise ValueError("nothing left of the output after the crop")
+    dims = (N, C_in, H, W, C_out, groups, KH, KW, sh, sw, pbh, pbw, pah, paw, oph, opw,
+            dh, dw)
+    return x, w, b, dims, (N, C_out, OH, OW)
+
+
+def conv_transpose2d(x, w, b=None, stride=1, pad_before=0, pad_after=None,
+                     output_padding=0, groups=1, dilation=1):
+    """Reference transposed convolution (w is [C_in, C_out/groups, KH, KW]).
+    Returns (y, bound) as float64 arrays of shape [N, C_out, OH, OW]."""
+    x, w, b, dims, oshape = _prep_transposed(x, w, b, stride, pad_before, pad_after,
+                                             output_padding, groups, dilation)
+    y = np.empty(oshape, dtype=np.float64)
+    bound = np.empty(oshape, dtype=np.float64)
+    rc = _load().oracle_conv_transpose2d_f64(_ptr(x), _ptr(w), _ptr(b), *dims, _ptr(y),
+                                             _ptr(bound))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return y, bound
+
+
+def conv_transpose2d_points(x, w, b, stride, pad_before, pad_after, output_padding,
+                            groups, pts, dilation=1):
+    """Transposed-convolution reference values at the (n, co, oh, ow) rows of
+    ``pts``.  Returns (y, bound), each of length P."""
+    x, w, b, dims, _ = _prep_transposed(x, w, b, stride, pad_before, pad_after,
+                                        output_padding, groups, dilation)
+    pts = np.ascontiguousarray(np.asarray(pts, dtype=np.int64).reshape(-1, 4))
+    y = np.empty(len(pts), dtype=np.float64)
+    bound = np.empty(len(pts), dtype=np.float64)
+    rc = _load().oracle_conv_transpose2d_f64_points(
+        _ptr(x), _ptr(w), _ptr(b), *dims, len(pts),
+        pts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _ptr(y), _ptr(bound))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments or a point")
+    return y, bound
+
+
+def conv2d_backward(x, w, gy, stride=1, pad_before=0, pad_after=None, groups=1,
+                    dilation=1, need=("dx", "dw", "db")):
+    """Gradients of the forward convolution for the output gradient ``gy``
+    ([N, C_out, OH, OW]).  Returns a dict with the requested entries among
+    "dx" [N, C_in, H, W], "dw" [C_out, Cin_g, KH, KW] and "db" [C_out], each a
+    (value, bound) pair of float64 arrays."""
+    unbatched = _as_f64(x).ndim == 3
+    x, w, _, dims, oshape = _prep(x, w, None, stride, pad_before, pad_after, groups,
+                                  dilation)
+    gy = _as_f64(gy)
+    if unbatched and gy.ndim == 3:
+        gy = gy[None]
+    if gy.shape != oshape:
+        raise ValueError(f"gy must be {oshape}")
+    out = {}
+    bufs = {}
+    shapes = {"dx": x.shape, "dw": w.shape, "db": (w.shape[0],)}
+    for k in ("dx", "dw", "db"):
+        if k in need:
+            bufs[k] = (np.empty(shapes[k]), np.empty(shapes[k]))
+        else:
+            bufs[k] = (None, None)
+    rc = _load().oracle_conv2d_backward_f64(
+        _ptr(x), _ptr(w), _ptr(gy), *dims,
+        _ptr(bufs["dx"][0]), _ptr(bufs["dx"][1]), _ptr(bufs["dw"][0]),
+        _ptr(bufs["dw"][1]), _ptr(bufs["db"][0]), _ptr(bufs["db"][1]))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    for k in need:
+        v, bnd = bufs[k]
+        if k == "dx" and unbatched:
+            v, bnd = v[0], bnd[0]
+        out[k] = (v, bnd)
+    return out
+
+
+# 1-D convolutions are the H = 1 case of the 2-D definitions: x [N, C, L]
+# (or [C, L]) becomes [N, C, 1, L] and w [Co, Cig, K] becomes [Co, Cig, 1, K].
+
+def _to_2d(x, w):
+    x = _as_f64(x)
+    w = _as_f64(w)
+    if x.ndim == 2:
+        x = x[None]
+    if x.ndim != 3 or w.ndim != 3:
+        raise ValueError("x must be [N,C,L] (or [C,L]); w must be rank 3")
+    return x[:, :, None, :], w[:, :, None, :]
+
+
+def conv1d(x, w, b=None, stride=1, pad_before=0, pad_after=None, groups=1, dilation=1):
+    """1-D reference convolution.  Returns (y, bound) of shape [N, C_out, OL]."""
+    x2, w2 = _to_2d(x, w)
+    pa = pad_before if pad_after is None else pad_after
+    y, bound = conv2d(x2, w2, b, (1, stride), (0, pad_before), (0, pa), groups,
+                      (1, dilation))
+    return y[:, :, 0, :], bound[:, :, 0, :]
+
+
+def conv_transpose1d(x, w, b=None, stride=1, pad_before=0, pad_after=None,
+                     output_padding=0, groups=1, dilation=1):
+    """1-D reference transposed convolution (w [C_in, C_out/groups, K])."""
+    x2, w2 = _to_2d(x, w)
+    pa = pad_before if pad_after is None else pad_after
+    y, bound = conv_transpose2d(x2, w2, b, (1, stride), (0, pad_before), (0, pa),
+                                (0, output_padding), groups, (1, dilation))
+    return y[:, :, 0, :], bound[:, :, 0, :]
 
 
 def violations(got, ref, bound, dtype: str):
