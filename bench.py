@@ -65,13 +65,14 @@ def run_case(args):
     gc.build()
     wl = WORKLOADS[args.case]
     x, w, b = make_inputs(wl, device="cuda")
-    for _ in range(args.reps):
-        y = gc.conv2d(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.groups,
-                      schedule=args.schedule)
-    torch.cuda.synchronize()
-    d = gc.conv_bind(x, w, b, wl.stride, wl.pad_before, wl.pad_after, 1, wl.groups)
+    d = gc.bind(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.dilation, wl.groups,
+                wl.transposed, wl.output_padding)
     if args.schedule:
         d.schedule = gc.SCHEDULES[args.schedule]
+    y = gc.empty_output(d, x)
+    for _ in range(args.reps):
+        gc.run(d, x, w, b, y)
+    torch.cuda.synchronize()
     print(json.dumps({"case": args.case, "reps": args.reps, "shape": list(y.shape),
                       "schedule": gc.conv_select_schedule(d, x, w, b, y)}))
 
@@ -118,12 +119,17 @@ def measured_peaks():
 
 
 def algorithmic(desc, elem):
-    """Bytes (x + w + bias + y, each once), FMAs and output pixels of one conv."""
+    """Bytes (x + w + bias + y, each once), FMAs and output pixels of one conv.
+    A transposed convolution's FMAs are its input's scatter: every input
+    element meets Cout_g * KH * KW weights (before the crop)."""
     x = desc.N * desc.C_in * desc.H * desc.W
     w = desc.C_out * desc.Cin_g * desc.KH * desc.KW
     b = desc.C_out if desc.has_bias else 0
     y = desc.N * desc.C_out * desc.OH * desc.OW
-    fma = y * desc.Cin_g * desc.KH * desc.KW
+    if desc.transposed:
+        fma = x * desc.Cout_g * desc.KH * desc.KW
+    else:
+        fma = y * desc.Cin_g * desc.KH * desc.KW
     return (x + w + b + y) * elem, fma, desc.N * desc.OH * desc.OW
 
 
@@ -231,8 +237,9 @@ class ConvCase:
         self.x_host = x
         self.w = w.to(device)
         self.b = b.to(device) if b is not None else None
-        self.desc = gc.conv_bind(x, w, b, self.wl.stride, self.wl.pad_before,
-                                 self.wl.pad_after, 1, self.wl.groups)
+        wl = self.wl
+        self.desc = gc.bind(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.dilation,
+                            wl.groups, wl.transposed, wl.output_padding)
         if schedule is not None:
             self.desc.schedule = gc.SCHEDULES[schedule]
         xd = x.to(device)
@@ -240,7 +247,6 @@ class ConvCase:
         self.ys = [gc.empty_output(self.desc, xd) for _ in range(sets)]
         self.elem = x.element_size()
         self.bytes, self.fma, self.pix = algorithmic(self.desc, self.elem)
-        self.fwd = gc.conv_dw_forward if self.desc.Cin_g == 1 else gc.conv_grouped_forward
         self.schedule = gc.conv_select_schedule(self.desc, self.xs[0], self.w, self.b, self.ys[0])
 
     def footprint(self):
@@ -248,7 +254,63 @@ class ConvCase:
 
     def run(self, i, stream=None):
         k = i % len(self.xs)
-        self.fwd(self.desc, self.xs[k], self.w, self.b, self.ys[k], stream)
+        self.gc.run(self.desc, self.xs[k], self.w, self.b, self.ys[k], stream)
+
+
+class BackwardCase:
+    """The backward of one forward workload: ``part`` "input" (dx from gy and
+    w) or "weight" (dw and db from x and gy, with the fp32 workspace), bound
+    once, with R rotating sets of its streamed tensors."""
+
+    def __init__(self, name, sets, device, part):
+        import torch
+        import grouped_convolution_gb300 as gc
+        from grouped_convolution_gb300.inputs import WORKLOADS, make_grad, make_inputs
+        self.gc = gc
+        self.part = part
+        self.wl = wl = WORKLOADS[name]
+        x, w, _ = make_inputs(wl)
+        self.desc = d = gc.conv_bind(x, w, None, wl.stride, wl.pad_before, wl.pad_after,
+                                     wl.dilation, wl.groups)
+        ysz, _ = gc.out_shape_and_stride(d)
+        gy = make_grad(wl, ysz)
+        self.w = w.to(device)
+        elem = x.element_size()
+        n_x, n_y, n_w = x.numel(), gy.numel(), w.numel()
+        self.pix = d.N * d.OH * d.OW
+        taps = d.Cin_g * d.KH * d.KW
+        self.fma = n_y * taps
+        xd, gyd = x.to(device), gy.to(device)
+        if part == "input":
+            sizes, strides = gc.grad_input_shape_and_stride(d)
+            self.gys = [gyd] + [gyd.clone() for _ in range(sets - 1)]
+            self.dxs = [torch.empty_strided(sizes, strides, dtype=x.dtype, device=device)
+                        for _ in range(sets)]
+            self.bytes = (n_y + n_w + n_x) * elem
+            self.streamed = self.gys + self.dxs
+        else:
+            self.xs = [xd] + [xd.clone() for _ in range(sets - 1)]
+            self.gys = [gyd] + [gyd.clone() for _ in range(sets - 1)]
+            self.dw = torch.empty(tuple(w.shape), dtype=x.dtype, device=device)
+            self.db = torch.empty(d.C_out, dtype=x.dtype, device=device)
+            self.ws_bytes = gc.conv_backward_weight_workspace_size(d)
+            self.ws = torch.empty((self.ws_bytes + 15) // 16 * 4, dtype=torch.float32,
+                                  device=device)
+            self.bytes = (n_x + n_y + n_w + d.C_out) * elem
+            self.streamed = self.xs + self.gys
+        self.elem = elem
+        self.schedule = f"backward_{part}"
+
+    def footprint(self):
+        return sum(t.numel() * t.element_size() for t in self.streamed)
+
+    def run(self, i, stream=None):
+        k = i % len(self.gys)
+        if self.part == "input":
+            self.gc.conv_backward_input(self.desc, self.gys[k], self.w, self.dxs[k], stream)
+        else:
+            self.gc.conv_backward_weight(self.desc, self.xs[k], self.gys[k], self.dw, self.db,
+                                         self.ws, self.ws_bytes, stream)
 
 
 def sets_needed(bytes_per_set, l2_bytes):
@@ -330,7 +392,7 @@ def time_e2e(cases, steps, world, lanes=3):
         with torch.cuda.stream(streams[k]):
             dev_x[k].copy_(host_x, non_blocking=True)
             for c, y, o in zip(cases, dev_y[k], outs[k]):
-                c.fwd(c.desc, dev_x[k], c.w, c.b, y, streams[k])
+                c.gc.run(c.desc, dev_x[k], c.w, c.b, y, streams[k])
                 o.copy_(y, non_blocking=True)
 
     for i in range(3 * lanes):  # warm-up
@@ -465,6 +527,25 @@ def per_config(args, world, l2, hbm_peak, dev):
         torch.cuda.empty_cache()
         return res
 
+    def measure_bwd(name, part):
+        one = BackwardCase(name, 1, dev, part)
+        R = sets_needed(one.footprint(), l2)
+        del one
+        torch.cuda.empty_cache()
+        c = BackwardCase(name, R, dev, part)
+        ms, _ = time_graph([c], steps, max(3, min(args.warmup, 50)), world)
+        t = ms / steps * 1e-3
+        gbs = c.bytes / t / 1e9
+        fma_peak = SMS * FMA_LANES * MAX_MHZ * 1e6
+        res = {"pass": part, "us": round(t * 1e6, 3), "GB_s": round(gbs, 1),
+               "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+               "TFMA_s": round(c.fma / t / 1e12, 3),
+               "frac_of_fma_peak_2070mhz": round(c.fma / t / fma_peak, 4),
+               "bytes": c.bytes, "fma": c.fma, "launches_per_call": 1 if part == "input" else 2}
+        del c
+        torch.cuda.empty_cache()
+        return res
+
     for name in WORKLOADS:
         out[name] = measure(name)
         # A call the picker sends to the tensor cores is also timed on the
@@ -474,6 +555,12 @@ def per_config(args, world, l2, hbm_peak, dev):
             out[name]["direct_stencil"] = {k: st[k] for k in (
                 "schedule", "us", "GB_s", "frac_of_measured_hbm", "TFMA_s",
                 "frac_of_fma_peak_2070mhz")}
+    # The backward of the step's layers: dx (a transposed convolution of the
+    # output gradient) and dw + db (two launches: slice partials, then the
+    # fixed-order sum).
+    for name in STEP_WORKLOADS:
+        for part in ("input", "weight"):
+            out[f"{name}.backward_{part}"] = measure_bwd(name, part)
     return out
 
 

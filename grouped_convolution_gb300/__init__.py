@@ -1,13 +1,20 @@
-"""GB300 direct-stencil depthwise / few-channel grouped 2-D convolution.
+"""GB300 direct-stencil depthwise / few-channel grouped convolution: 2-D and
+1-D, any dilation, forward, transposed and backward.
 
 A thin Python binding over the C ABI in ``include/gconv.h`` (``libgconv.so``,
 hand-written sm_103a CUDA kernels).  This module only marshals arguments:
 every step of the convolution runs in the library's kernels, and there is no
 CPU fallback -- a missing library is an error.
 
-Functions keep the ABI's names: ``conv_bind``, ``out_shape_and_stride``,
-``conv_dw_forward``, ``conv_grouped_forward``, ``conv_select_schedule``,
-``conv_force_schedule``; ``conv2d`` strings them together for torch tensors.
+Functions keep the ABI's names: ``conv_bind``, ``conv1d_bind``,
+``conv_transpose_bind``, ``conv_transpose1d_bind``, ``out_shape_and_stride``,
+``grad_input_shape_and_stride``, ``conv_dw_forward``,
+``conv_grouped_forward``, ``conv_transpose_forward``,
+``conv_backward_input``, ``conv_backward_weight_workspace_size``,
+``conv_backward_weight``, ``conv_select_schedule``,
+``conv_force_schedule``; ``conv2d``, ``conv1d``, ``conv_transpose2d``,
+``conv_transpose1d`` and ``conv2d_backward`` string them together for torch
+tensors.
 """
 
 from __future__ import annotations
@@ -21,11 +28,14 @@ __all__ = [
     "build", "conv_bind", "out_shape_and_stride", "conv_dw_forward",
     "conv_grouped_forward", "conv_select_schedule", "conv_force_schedule",
     "conv_schedule_name", "conv_strerror", "conv_launch_count", "conv2d",
-    "GconvError", "SCHEDULES", "lib_path",
+    "conv1d_bind", "conv_transpose_bind", "conv_transpose1d_bind", "conv_transpose_forward",
+    "grad_input_shape_and_stride", "conv_backward_input", "conv_backward_weight_workspace_size",
+    "conv_backward_weight", "conv1d", "conv_transpose2d", "conv_transpose1d",
+    "conv2d_backward", "GconvError", "SCHEDULES", "lib_path",
 ]
 
 SCHEDULES = {"auto": -1, "dw_flat": 0, "dw_row8": 1, "dw_mult": 2,
-             "grp_plane": 3, "grp_reduce": 4, "grp_tc": 5}
+             "grp_plane": 3, "grp_reduce": 4, "grp_tc": 5, "dw_line": 6}
 _DTYPE_CODES = {"float32": 0, "float16": 1, "bfloat16": 2}
 
 _lock = threading.Lock()
@@ -56,7 +66,9 @@ class Desc(ctypes.Structure):
         ("pad_after", ctypes.c_int32 * 2),
         ("x_strides", ctypes.c_int64 * 4), ("w_strides", ctypes.c_int64 * 4),
         ("b_stride", ctypes.c_int64), ("y_strides", ctypes.c_int64 * 4),
-        ("x_dense", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("x_dense", ctypes.c_int32), ("transposed", ctypes.c_int32),
+        ("spatial_dims", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("dilation", ctypes.c_int32 * 2), ("output_padding", ctypes.c_int32 * 2),
     ]
 
 
@@ -86,11 +98,27 @@ def _load():
         lib.conv_bind.restype = i32
         lib.conv_bind.argtypes = [P(Tensor), P(Tensor), P(Tensor), i32, P(i32), P(i32),
                                   P(i32), P(i32), i64, P(Desc)]
-        lib.out_shape_and_stride.restype = i32
-        lib.out_shape_and_stride.argtypes = [P(Desc), P(i32), P(i64), P(i64)]
-        for fn in (lib.conv_dw_forward, lib.conv_grouped_forward):
+        lib.conv1d_bind.restype = i32
+        lib.conv1d_bind.argtypes = [P(Tensor), P(Tensor), P(Tensor), i32, i32, i32, i32, i32,
+                                    i64, P(Desc)]
+        lib.conv_transpose_bind.restype = i32
+        lib.conv_transpose_bind.argtypes = [P(Tensor), P(Tensor), P(Tensor), i32, P(i32), P(i32),
+                                            P(i32), P(i32), P(i32), i64, P(Desc)]
+        lib.conv_transpose1d_bind.restype = i32
+        lib.conv_transpose1d_bind.argtypes = [P(Tensor), P(Tensor), P(Tensor), i32, i32, i32,
+                                              i32, i32, i32, i64, P(Desc)]
+        for fn in (lib.out_shape_and_stride, lib.grad_input_shape_and_stride):
+            fn.restype = i32
+            fn.argtypes = [P(Desc), P(i32), P(i64), P(i64)]
+        for fn in (lib.conv_dw_forward, lib.conv_grouped_forward, lib.conv_transpose_forward):
             fn.restype = i32
             fn.argtypes = [P(Desc), vp, vp, vp, vp, vp]
+        lib.conv_backward_input.restype = i32
+        lib.conv_backward_input.argtypes = [P(Desc), vp, vp, vp, vp]
+        lib.conv_backward_weight_workspace_size.restype = i32
+        lib.conv_backward_weight_workspace_size.argtypes = [P(Desc), P(ctypes.c_uint64)]
+        lib.conv_backward_weight.restype = i32
+        lib.conv_backward_weight.argtypes = [P(Desc), vp, vp, vp, vp, vp, ctypes.c_uint64, vp]
         lib.conv_select_schedule.restype = i32
         lib.conv_select_schedule.argtypes = [P(Desc), vp, vp, vp, vp, P(i32)]
         lib.conv_force_schedule.restype = i32
@@ -149,23 +177,31 @@ def _dtype_code(dtype) -> int:
     return _DTYPE_CODES[name]
 
 
+def _geo(t):
+    if t is None:
+        return None
+    if isinstance(t, tuple):
+        return geometry(*t)
+    return geometry(t.shape, t.stride())
+
+
+def _common_dtype(x, w, bias, dtype):
+    if dtype is not None:
+        return dtype
+    dtype = x.dtype
+    for t in (w, bias):
+        if t is not None and not isinstance(t, tuple) and t.dtype != dtype:
+            raise GconvError(3, "x, w and bias must share one dtype")
+    return dtype
+
+
 def conv_bind(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
               dilation=1, groups=1, dtype=None) -> Desc:
     """Validate and canonicalise one convolution.  ``x``, ``w`` and ``bias``
     may be torch tensors or ``(sizes, strides)`` pairs (then ``dtype`` names
     the element type).  Returns the ABI's ``gconv_desc``."""
-    def geo(t):
-        if t is None:
-            return None
-        if isinstance(t, tuple):
-            return geometry(*t)
-        return geometry(t.shape, t.stride())
-    if dtype is None:
-        dtype = x.dtype
-        for t in (w, bias):
-            if t is not None and not isinstance(t, tuple) and t.dtype != dtype:
-                raise GconvError(3, "x, w and bias must share one dtype")
-    xs, ws, bs = geo(x), geo(w), geo(bias)
+    dtype = _common_dtype(x, w, bias, dtype)
+    xs, ws, bs = _geo(x), _geo(w), _geo(bias)
     arr = ctypes.c_int32 * 2
     st = arr(*_pair(stride, "stride"))
     pb = arr(*_pair(padding_before, "padding_before"))
@@ -180,6 +216,58 @@ def conv_bind(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
     return d
 
 
+def conv1d_bind(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
+                dilation=1, groups=1, dtype=None) -> Desc:
+    """1-D convolution: x [N, C, L] (or [C, L]), w [C_out, Cin_g, K]."""
+    dtype = _common_dtype(x, w, bias, dtype)
+    xs, ws, bs = _geo(x), _geo(w), _geo(bias)
+    pa = padding_before if padding_after is None else padding_after
+    d = Desc()
+    rc = _load().conv1d_bind(ctypes.byref(xs), ctypes.byref(ws),
+                             ctypes.byref(bs) if bs is not None else None, _dtype_code(dtype),
+                             int(stride), int(padding_before), int(pa), int(dilation),
+                             int(groups), ctypes.byref(d))
+    _check(rc, "conv1d_bind")
+    return d
+
+
+def conv_transpose_bind(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
+                        output_padding=0, dilation=1, groups=1, dtype=None) -> Desc:
+    """Transposed 2-D convolution: w is [C_in, C_out/groups, KH, KW]."""
+    dtype = _common_dtype(x, w, bias, dtype)
+    xs, ws, bs = _geo(x), _geo(w), _geo(bias)
+    arr = ctypes.c_int32 * 2
+    st = arr(*_pair(stride, "stride"))
+    pb = arr(*_pair(padding_before, "padding_before"))
+    pa = arr(*_pair(padding_before if padding_after is None else padding_after,
+                    "padding_after"))
+    op = arr(*_pair(output_padding, "output_padding"))
+    dl = arr(*_pair(dilation, "dilation"))
+    d = Desc()
+    rc = _load().conv_transpose_bind(ctypes.byref(xs), ctypes.byref(ws),
+                                     ctypes.byref(bs) if bs is not None else None,
+                                     _dtype_code(dtype), st, pb, pa, op, dl, int(groups),
+                                     ctypes.byref(d))
+    _check(rc, "conv_transpose_bind")
+    return d
+
+
+def conv_transpose1d_bind(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
+                          output_padding=0, dilation=1, groups=1, dtype=None) -> Desc:
+    """Transposed 1-D convolution: x [N, C_in, L] (or [C_in, L]), w [C_in, Cog, K]."""
+    dtype = _common_dtype(x, w, bias, dtype)
+    xs, ws, bs = _geo(x), _geo(w), _geo(bias)
+    pa = padding_before if padding_after is None else padding_after
+    d = Desc()
+    rc = _load().conv_transpose1d_bind(ctypes.byref(xs), ctypes.byref(ws),
+                                       ctypes.byref(bs) if bs is not None else None,
+                                       _dtype_code(dtype), int(stride), int(padding_before),
+                                       int(pa), int(output_padding), int(dilation), int(groups),
+                                       ctypes.byref(d))
+    _check(rc, "conv_transpose1d_bind")
+    return d
+
+
 def out_shape_and_stride(desc: Desc):
     """Output (sizes, strides) in elements, as the ABI computes them."""
     rank = ctypes.c_int32()
@@ -187,6 +275,17 @@ def out_shape_and_stride(desc: Desc):
     strides = (ctypes.c_int64 * 4)()
     _check(_load().out_shape_and_stride(ctypes.byref(desc), ctypes.byref(rank), sizes, strides),
            "out_shape_and_stride")
+    r = rank.value
+    return tuple(sizes[:r]), tuple(strides[:r])
+
+
+def grad_input_shape_and_stride(desc: Desc):
+    """(sizes, strides) of dx for a forward desc: x's sizes, dense in its layout."""
+    rank = ctypes.c_int32()
+    sizes = (ctypes.c_int64 * 4)()
+    strides = (ctypes.c_int64 * 4)()
+    _check(_load().grad_input_shape_and_stride(ctypes.byref(desc), ctypes.byref(rank), sizes,
+                                               strides), "grad_input_shape_and_stride")
     r = rank.value
     return tuple(sizes[:r]), tuple(strides[:r])
 
@@ -219,6 +318,35 @@ def conv_grouped_forward(desc: Desc, x, w, bias, y, stream=None):
     """Grouped forward (1..8 input channels per group) into ``y``."""
     _check(_load().conv_grouped_forward(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias),
                                         _ptr(y), _stream_ptr(stream)), "conv_grouped_forward")
+
+
+def conv_transpose_forward(desc: Desc, x, w, bias, y, stream=None):
+    """Transposed forward into ``y`` (desc from conv_transpose[1d]_bind)."""
+    _check(_load().conv_transpose_forward(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias),
+                                          _ptr(y), _stream_ptr(stream)), "conv_transpose_forward")
+
+
+def conv_backward_input(desc: Desc, gy, w, dx, stream=None):
+    """dx for the forward desc, into the preallocated ``dx``."""
+    _check(_load().conv_backward_input(ctypes.byref(desc), _ptr(gy), _ptr(w), _ptr(dx),
+                                       _stream_ptr(stream)), "conv_backward_input")
+
+
+def conv_backward_weight_workspace_size(desc: Desc) -> int:
+    out = ctypes.c_uint64()
+    _check(_load().conv_backward_weight_workspace_size(ctypes.byref(desc), ctypes.byref(out)),
+           "conv_backward_weight_workspace_size")
+    return int(out.value)
+
+
+def conv_backward_weight(desc: Desc, x, gy, dw, db, workspace, workspace_bytes=None,
+                         stream=None):
+    """dw (dense [C_out, Cin_g, KH, KW]) and db (dense [C_out], or None)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(_load().conv_backward_weight(ctypes.byref(desc), _ptr(x), _ptr(gy), _ptr(dw),
+                                        _ptr(db), _ptr(workspace), int(workspace_bytes),
+                                        _stream_ptr(stream)), "conv_backward_weight")
 
 
 def conv_select_schedule(desc: Desc, x, w, bias, y) -> str:
@@ -268,11 +396,11 @@ def empty_output(desc: Desc, like):
 
 
 def conv2d(x, w, bias=None, stride=1, padding_before=0, padding_after=None, groups=1,
-           schedule=None, out=None, stream=None):
+           schedule=None, out=None, stream=None, dilation=1):
     """Bind, allocate the output and run the forward on CUDA tensors."""
     if not (x.is_cuda and w.is_cuda and (bias is None or bias.is_cuda)):
         raise GconvError(1, "conv2d needs CUDA tensors (there is no CPU path)")
-    d = conv_bind(x, w, bias, stride, padding_before, padding_after, 1, groups)
+    d = conv_bind(x, w, bias, stride, padding_before, padding_after, dilation, groups)
     if schedule is not None:
         d.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     y = empty_output(d, x) if out is None else out
@@ -281,3 +409,110 @@ def conv2d(x, w, bias=None, stride=1, padding_before=0, padding_after=None, grou
     else:
         conv_grouped_forward(d, x, w, bias, y, stream)
     return y
+
+
+def _cuda_only(*ts):
+    if not all(t is None or t.is_cuda for t in ts):
+        raise GconvError(1, "needs CUDA tensors (there is no CPU path)")
+
+
+def _forced(d, schedule):
+    if schedule is not None:
+        d.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
+
+
+def conv1d(x, w, bias=None, stride=1, padding_before=0, padding_after=None, groups=1,
+           dilation=1, schedule=None, out=None, stream=None):
+    """1-D forward on CUDA tensors: x [N, C, L], w [C_out, Cin_g, K]."""
+    _cuda_only(x, w, bias)
+    d = conv1d_bind(x, w, bias, stride, padding_before, padding_after, dilation, groups)
+    _forced(d, schedule)
+    y = empty_output(d, x) if out is None else out
+    conv_grouped_forward(d, x, w, bias, y, stream)
+    return y
+
+
+def conv_transpose2d(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
+                     output_padding=0, groups=1, dilation=1, schedule=None, out=None,
+                     stream=None):
+    """Transposed 2-D forward on CUDA tensors: w [C_in, C_out/groups, KH, KW]."""
+    _cuda_only(x, w, bias)
+    d = conv_transpose_bind(x, w, bias, stride, padding_before, padding_after, output_padding,
+                            dilation, groups)
+    _forced(d, schedule)
+    y = empty_output(d, x) if out is None else out
+    conv_transpose_forward(d, x, w, bias, y, stream)
+    return y
+
+
+def conv_transpose1d(x, w, bias=None, stride=1, padding_before=0, padding_after=None,
+                     output_padding=0, groups=1, dilation=1, schedule=None, out=None,
+                     stream=None):
+    """Transposed 1-D forward on CUDA tensors: w [C_in, C_out/groups, K]."""
+    _cuda_only(x, w, bias)
+    d = conv_transpose1d_bind(x, w, bias, stride, padding_before, padding_after,
+                              output_padding, dilation, groups)
+    _forced(d, schedule)
+    y = empty_output(d, x) if out is None else out
+    conv_transpose_forward(d, x, w, bias, y, stream)
+    return y
+
+
+def conv2d_backward(x, w, gy, stride=1, padding_before=0, padding_after=None, groups=1,
+                    dilation=1, need=("dx", "dw", "db"), schedule=None, stream=None):
+    """Gradients of the 2-D forward for the output gradient ``gy`` (CUDA
+    tensors).  Returns a dict with the requested "dx", "dw", "db"."""
+    _cuda_only(x, w, gy)
+    import torch
+    d = conv_bind(x, w, None, stride, padding_before, padding_after, dilation, groups)
+    _forced(d, schedule)
+    out = {}
+    if "dx" in need:
+        sizes, strides = grad_input_shape_and_stride(d)
+        dx = torch.empty_strided(sizes, strides, dtype=x.dtype, device=x.device)
+        conv_backward_input(d, gy, w, dx, stream)
+        out["dx"] = dx
+    if "dw" in need or "db" in need:
+        dw = torch.empty(tuple(w.shape), dtype=x.dtype, device=x.device)
+        db = torch.empty(d.C_out, dtype=x.dtype, device=x.device) if "db" in need else None
+        nbytes = conv_backward_weight_workspace_size(d)
+        ws = torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=x.device)
+        conv_backward_weight(d, x, gy, dw, db, ws, nbytes, stream)
+        if "dw" in need:
+            out["dw"] = dw
+        if db is not None:
+            out["db"] = db
+    return out
+
+
+def bind(x, w, bias=None, stride=1, padding_before=0, padding_after=None, dilation=1,
+         groups=1, transposed=False, output_padding=0, dtype=None) -> Desc:
+    """Any of the four bindings, chosen by the weight's rank (3: 1-D, 4: 2-D)
+    and ``transposed``.  For 1-D calls, (h, w) pairs give their w element."""
+    def last(v):
+        return v if isinstance(v, int) else int(tuple(v)[-1])
+    w_rank = len(w[0]) if isinstance(w, tuple) else w.dim()
+    if w_rank == 3:
+        pa = padding_before if padding_after is None else padding_after
+        if transposed:
+            return conv_transpose1d_bind(x, w, bias, last(stride), last(padding_before),
+                                         last(pa), last(output_padding), last(dilation),
+                                         groups, dtype)
+        return conv1d_bind(x, w, bias, last(stride), last(padding_before), last(pa),
+                           last(dilation), groups, dtype)
+    if transposed:
+        return conv_transpose_bind(x, w, bias, stride, padding_before, padding_after,
+                                   output_padding, dilation, groups, dtype)
+    return conv_bind(x, w, bias, stride, padding_before, padding_after, dilation, groups,
+                     dtype)
+
+
+def run(desc: Desc, x, w, bias, y, stream=None):
+    """The forward entry point that takes this desc (transposed, depthwise
+    or grouped)."""
+    if desc.transposed:
+        conv_transpose_forward(desc, x, w, bias, y, stream)
+    elif desc.Cin_g == 1:
+        conv_dw_forward(desc, x, w, bias, y, stream)
+    else:
+        conv_grouped_forward(desc, x, w, bias, y, stream)

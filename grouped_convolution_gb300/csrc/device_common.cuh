@@ -55,6 +55,24 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half *) {
 template <typename T>
 __device__ __forceinline__ float load_f32(const T *p) { return Elem<T>::load(p); }
 
+// The input index that output index o reads at tap k along one dim, or -1
+// when the tap falls outside the input.  Forward: o*s - pb + k*d (the conv.py
+// LOOP_BODY_2D rule with dilation).  Transposed (executorch PR #25091,
+// description, second paragraph): (o + pb - k*d) / s when that is a whole
+// number.
+template <bool TR>
+__device__ __forceinline__ int tap_input(int o, int k, int s, int pb, int d, int n_in) {
+    if constexpr (!TR) {
+        const int i = o * s - pb + k * d;
+        return (i >= 0 && i < n_in) ? i : -1;
+    } else {
+        const int t = o + pb - k * d;
+        if (t < 0) return -1;
+        const int i = t / s;
+        return (i * s == t && i < n_in) ? i : -1;
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ T from_f32(float v) { return Elem<T>::from_f32(v); }
 

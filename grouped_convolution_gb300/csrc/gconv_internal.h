@@ -16,6 +16,8 @@ constexpr uint32_t kDescMagic = 0x47434f4eu;  // "GCON"
 struct Params {
     int N, C_in, H, W, C_out, G, Cin_g, Cout_g, KH, KW, OH, OW;
     int sh, sw, pbh, pbw;
+    int dh, dw;      // dilation
+    int transposed;  // 1: y gathers x at (o + pb - k*d) / s (weight [C_in, Cout_g, KH, KW])
     int has_bias, layout, dtype;
     int64_t xs[4];   // x strides, logical (N, C, H, W)
     int64_t ws[4];   // w strides, logical (C_out, Cin_g, KH, KW)
@@ -47,6 +49,18 @@ extern const Schedule kDwMult;
 extern const Schedule kGrpPlane;
 extern const Schedule kGrpReduce;
 extern const Schedule kGrpTc;
+extern const Schedule kDwLine;
+
+// The plain forward convolution of the direct-stencil envelope (dilation 1,
+// not transposed): the only calls the specialised schedules take.
+inline bool plain_forward(const gconv_desc &d) {
+    return !d.transposed && d.dilation[0] == 1 && d.dilation[1] == 1;
+}
+
+// Backward weight pass (k_wgrad.cu): workspace bytes, and the launches.
+uint64_t wgrad_workspace_bytes(const Params &p);
+cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *dw, void *db,
+                         void *workspace, cudaStream_t s, int *launches);
 
 inline bool aligned(const void *p, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;

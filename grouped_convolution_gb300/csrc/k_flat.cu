@@ -3,8 +3,11 @@
 //
 // One thread per output element, threads numbered in y's memory order so
 // stores are coalesced in either layout.  x, w and bias are read through
-// their strides, so every layout, group shape (Cin_g <= 8, any Cout_g) and
-// multiplier runs here; the specialised schedules cover the hot shapes.
+// their strides, so every layout, group shape (Cin_g <= 8, any Cout_g),
+// multiplier and dilation runs here, forward or transposed (the transposed
+// gather of executorch PR #25091, description, second paragraph, with the
+// [C_in, Cout_g, KH, KW] weight); the specialised schedules cover the hot
+// shapes.
 // Accumulation is fp32 in (ci, kh, kw) order; the epilogue adds the bias and
 // rounds once to the output dtype.
 
@@ -15,7 +18,7 @@
 namespace gconv {
 namespace {
 
-template <typename T, typename I>
+template <typename T, typename I, bool TR>
 __global__ void __launch_bounds__(256)
 flat_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
             T *__restrict__ y, Params p, int64_t total) {
@@ -40,19 +43,21 @@ flat_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
         }
         const int g = (int)(co / p.Cout_g);
         const T *xn = x + (int64_t)n * p.xs[0] + (int64_t)g * p.Cin_g * p.xs[1];
-        const T *wc = w + (int64_t)co * p.ws[0];
-        const int ih0 = (int)oh * p.sh - p.pbh;
-        const int iw0 = (int)ow * p.sw - p.pbw;
+        // Weight of (co, ci): w[co, ci] forward, w[g*Cin_g + ci, co - g*Cout_g]
+        // transposed.
+        const T *wc = TR ? w + (int64_t)g * p.Cin_g * p.ws[0] + (int64_t)(co - g * p.Cout_g) * p.ws[1]
+                         : w + (int64_t)co * p.ws[0];
+        const int64_t wci = TR ? p.ws[0] : p.ws[1];
         float acc = 0.f;
         for (int ci = 0; ci < p.Cin_g; ++ci) {
             for (int kh = 0; kh < p.KH; ++kh) {
-                const int ih = ih0 + kh;
-                if (ih < 0 || ih >= p.H) continue;
+                const int ih = tap_input<TR>((int)oh, kh, p.sh, p.pbh, p.dh, p.H);
+                if (ih < 0) continue;
                 for (int kw = 0; kw < p.KW; ++kw) {
-                    const int iw = iw0 + kw;
-                    if (iw < 0 || iw >= p.W) continue;
+                    const int iw = tap_input<TR>((int)ow, kw, p.sw, p.pbw, p.dw, p.W);
+                    if (iw < 0) continue;
                     const float xv = load_f32(xn + ci * p.xs[1] + ih * p.xs[2] + iw * p.xs[3]);
-                    const float wv = load_f32(wc + ci * p.ws[1] + kh * p.ws[2] + kw * p.ws[3]);
+                    const float wv = load_f32(wc + ci * wci + kh * p.ws[2] + kw * p.ws[3]);
                     acc = fmaf(wv, xv, acc);
                 }
             }
@@ -76,12 +81,17 @@ cudaError_t flat_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *lau
         const T *b = static_cast<const T *>(q.b);
         T *y = static_cast<T *>(q.y);
         cudaError_t e;
-        if (total <= INT32_MAX)
-            e = launch_pdl(flat_kernel<T, int>, dim3((unsigned)blocks), dim3(threads), 0, s, x, w,
-                           b, y, p, total);
+        const bool small = total <= INT32_MAX;
+        if (p.transposed)
+            e = small ? launch_pdl(flat_kernel<T, int, true>, dim3((unsigned)blocks), dim3(threads),
+                                   0, s, x, w, b, y, p, total)
+                      : launch_pdl(flat_kernel<T, int64_t, true>, dim3((unsigned)blocks),
+                                   dim3(threads), 0, s, x, w, b, y, p, total);
         else
-            e = launch_pdl(flat_kernel<T, int64_t>, dim3((unsigned)blocks), dim3(threads), 0, s,
-                           x, w, b, y, p, total);
+            e = small ? launch_pdl(flat_kernel<T, int, false>, dim3((unsigned)blocks),
+                                   dim3(threads), 0, s, x, w, b, y, p, total)
+                      : launch_pdl(flat_kernel<T, int64_t, false>, dim3((unsigned)blocks),
+                                   dim3(threads), 0, s, x, w, b, y, p, total);
         (void)per_image;
         *launches = 1;
         return e != cudaSuccess ? e : cudaGetLastError();

@@ -6,6 +6,7 @@ namespace gconv {
 namespace {
 
 bool grp_supports(const gconv_desc &d, const Ptrs &q) {
+    if (!plain_forward(d)) return false;                    // dilation 1, forward
     (void)q;
     if (d.stride[1] != 1 && d.stride[1] != 2) return false;
     Params p = make_params(d);

@@ -6,6 +6,7 @@ namespace gconv {
 namespace {
 
 bool mult_supports(const gconv_desc &d, const Ptrs &q) {
+    if (!plain_forward(d)) return false;                    // dilation 1, forward
     if (d.Cin_g != 1 || d.Cout_g > 16) return false;
     if (d.layout != GCONV_LAYOUT_NCHW) return false;
     if (d.KW > kMultMaxKW) return false;

@@ -8,8 +8,10 @@
 // in fp32, reading x and w through their strides (any layout), and the L
 // partial sums are combined with xor shuffles.  Outputs are numbered in y's
 // memory order, so each group of lanes stores next to the previous group.
-// It takes every call and pays off when there are too few outputs to give
-// each thread its own (a small image or channel count with a big kernel).
+// It takes every call (any dilation, forward or transposed: the transposed
+// gather of executorch PR #25091, description, second paragraph) and pays
+// off when there are too few outputs to give each thread its own (a small
+// image or channel count with a big kernel).
 #include "device_common.cuh"
 #include "gconv_internal.h"
 #include "launch.cuh"
@@ -19,7 +21,7 @@ namespace {
 
 constexpr int kReduceThreads = 256;
 
-template <typename T, int L>
+template <typename T, int L, bool TR>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
               T *__restrict__ y, Params p, int64_t total) {
@@ -51,16 +53,20 @@ reduce_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restr
         }
         const int g = co / p.Cout_g;
         const T *xn = x + (int64_t)n * p.xs[0] + (int64_t)g * p.Cin_g * p.xs[1];
-        const T *wc = w + (int64_t)co * p.ws[0];
-        const int ih0 = oh * p.sh - p.pbh, iw0 = ow * p.sw - p.pbw;
+        // Weight of (co, ci): w[co, ci] forward, w[g*Cin_g + ci, co - g*Cout_g]
+        // transposed.
+        const T *wc = TR ? w + (int64_t)g * p.Cin_g * p.ws[0] + (int64_t)(co - g * p.Cout_g) * p.ws[1]
+                         : w + (int64_t)co * p.ws[0];
+        const int64_t wci = TR ? p.ws[0] : p.ws[1];
         float acc = 0.f;
         for (int tap = lane; valid && tap < taps; tap += L) {
             const int ci = tap / khw, k = tap - ci * khw;
             const int kh = k / p.KW, kw = k - kh * p.KW;
-            const int ih = ih0 + kh, iw = iw0 + kw;
-            if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) {
+            const int ih = tap_input<TR>(oh, kh, p.sh, p.pbh, p.dh, p.H);
+            const int iw = tap_input<TR>(ow, kw, p.sw, p.pbw, p.dw, p.W);
+            if (ih >= 0 && iw >= 0) {
                 const float xv = load_f32(xn + ci * p.xs[1] + ih * p.xs[2] + iw * p.xs[3]);
-                const float wv = load_f32(wc + ci * p.ws[1] + kh * p.ws[2] + kw * p.ws[3]);
+                const float wv = load_f32(wc + ci * wci + kh * p.ws[2] + kw * p.ws[3]);
                 acc = fmaf(wv, xv, acc);
             }
         }
@@ -89,12 +95,14 @@ cudaError_t reduce_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *l
         const T *b = static_cast<const T *>(q.b);
         T *y = static_cast<T *>(q.y);
         cudaError_t e;
-        if (wide)
-            e = launch_pdl(reduce_kernel<T, 32>, dim3((unsigned)blocks), dim3(kReduceThreads), 0, s,
-                           x, w, b, y, p, total);
+        auto go = [&](auto kernel) {
+            return launch_pdl(kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0, s, x, w, b,
+                              y, p, total);
+        };
+        if (p.transposed)
+            e = wide ? go(reduce_kernel<T, 32, true>) : go(reduce_kernel<T, 8, true>);
         else
-            e = launch_pdl(reduce_kernel<T, 8>, dim3((unsigned)blocks), dim3(kReduceThreads), 0, s,
-                           x, w, b, y, p, total);
+            e = wide ? go(reduce_kernel<T, 32, false>) : go(reduce_kernel<T, 8, false>);
         return e != cudaSuccess ? e : cudaGetLastError();
     });
 }

@@ -6,6 +6,7 @@ namespace gconv {
 namespace {
 
 bool row8_supports(const gconv_desc &d, const Ptrs &q) {
+    if (!plain_forward(d)) return false;                    // dilation 1, forward
     if (d.Cin_g != 1 || d.Cout_g != 1) return false;          // multiplier 1
     if (d.layout != GCONV_LAYOUT_NHWC) return false;          // channel-contiguous
     if (d.KH != d.KW) return false;

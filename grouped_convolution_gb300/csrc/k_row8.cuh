@@ -21,7 +21,8 @@
 //    pixels.  Its KH*KW weights (fp32 channel pairs) stay in registers for
 //    the CTA's lifetime.  Each staged input row is widened once into a
 //    window of (S-1)*S_W + KW vectors (32-bit shared addressing) and
-//    multiplied into every output row still open on it: R = ceil(KH / S_H)
+//    multiplied (packed fma.rn.f32x2 over channel pairs) into every output
+//    row still open on it: R = ceil(KH / S_H)
 //    accumulator sets rotate through the output rows, with set indices fixed
 //    at compile time by unrolling the row loop over one rotation period.
 //  - Accumulators start at the bias (fp32); a finished output row is
@@ -340,11 +341,8 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
 #pragma unroll
                         for (int kw = 0; kw < K; ++kw)
 #pragma unroll
-                            for (int k = 0; k < P; ++k)
-                                if constexpr (K >= 5)   // measured: packed wins for 5x5/7x7, scalar for 3x3
-                                    fma2_packed(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw][k]);
-                                else
-                                    fma2(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw][k]);
+                            for (int k = 0; k < P; ++k)   // packed: half the issue slots
+                                fma2_packed(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw][k]);
                 }
                 // The output row whose last tap row this was is done.
                 const int d = ph - (K - 1);

@@ -495,6 +495,7 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
 }
 
 bool tc_supports(const gconv_desc &d, const Ptrs &q) {
+    if (!plain_forward(d)) return false;                    // dilation 1, forward
     if (d.layout != GCONV_LAYOUT_NHWC) return false;
     if (d.dtype != GCONV_BF16 && d.dtype != GCONV_F16) return false;   // kind::f16 operands
     if (d.KH > 9 || d.KW > 9) return false;

@@ -1,0 +1,333 @@
+// k_wgrad.cu -- the backward pass for the weight and the bias:
+//   dw[co, ci, kh, kw] = sum_{n, oh, ow} gy[n, co, oh, ow] * x[n, g*Cin_g + ci, ih, iw]
+//   db[co]             = sum_{n, oh, ow} gy[n, co, oh, ow]
+// with (ih, iw) the forward taps (torch/_inductor/kernel/conv.py,
+// convolution_backward_lowering: grad weight, and grad bias as the sum of
+// grad_output over batch and space).
+//
+// Two launches.  The first splits the output pixels (n, oh, ow) into slices
+// and writes one fp32 partial sum per (slice, co, tap) -- bias as one more
+// tap -- into the caller's workspace [slice][C_out][Cin_g*KH*KW + 1]; the
+// second adds each entry's slices in fp64 in slice order and rounds once
+// into dw (dense [C_out, Cin_g, KH, KW]) and db.  No atomics: the result is
+// the same on every run.
+//
+// Partial pass, two forms:
+//  - channels-last depthwise (one input and one output channel per group):
+//    a block owns a chunk of channel vectors and a slice of pixels; lane
+//    (cv, pixel lane) keeps CH channels x every tap in fp32 registers, walks
+//    its pixels (one gy vector load, one x vector load per tap in the input,
+//    packed FMAs), and the block adds its pixel lanes in shared memory, one
+//    tap at a time in a fixed order;
+//  - any other layout or group shape: a block owns (slice, co), every thread
+//    sums a tap over its pixels through the strides, and a fixed-order block
+//    reduction (shuffles, then shared memory) gives the slice's value.
+#include "device_common.cuh"
+#include "gconv_internal.h"
+#include "launch.cuh"
+#include "stencil_math.cuh"
+
+namespace gconv {
+namespace {
+
+constexpr int kWgThreads = 256;
+constexpr int kWgBlocksTarget = 152 * 4;
+
+// Channels per lane for the channels-last form: all taps of CH channels in
+// registers (at most about 100 fp32 accumulators).
+template <typename T, int TMAX> constexpr int wg_ch() {
+    return TMAX <= 9 ? 16 / (int)sizeof(T) : (TMAX <= 25 ? 4 : 2);
+}
+
+struct WgPlan {
+    bool cl;          // channels-last depthwise form
+    int tmax;         // 9, 25 or 49 (cl form)
+    int ch;           // channels per lane (cl form)
+    int CVb, PL;      // lanes along channels / pixels (cl form)
+    int chunks;       // channel chunks (cl form)
+    int slices;
+    int64_t P;        // output pixels N * OH * OW
+    int T1;           // Cin_g * KH * KW + 1
+};
+
+int cl_tmax(const Params &p) {
+    const int taps = p.KH * p.KW;
+    return taps <= 9 ? 9 : (taps <= 25 ? 25 : (taps <= 49 ? 49 : 0));
+}
+
+int cl_ch(const Params &p, int tmax) {
+    const int es = dtype_size(p.dtype);
+    return tmax <= 9 ? 16 / es : (tmax <= 25 ? 4 : 2);
+}
+
+// The shape half of the channels-last test (the pointer half is in
+// wg_cl_pointers); the workspace size depends on the shape only.
+bool cl_shape(const Params &p) {
+    if (p.Cin_g != 1 || p.Cout_g != 1 || p.layout != GCONV_LAYOUT_NHWC) return false;
+    const int tmax = cl_tmax(p);
+    if (!tmax) return false;
+    const int ch = cl_ch(p, tmax);
+    if (p.C_out % ch) return false;
+    if (p.xs[1] != 1 || p.xs[0] % ch || p.xs[2] % ch || p.xs[3] % ch) return false;
+    if (p.ys[1] != 1 || p.ys[0] % ch || p.ys[2] % ch || p.ys[3] % ch) return false;
+    return (int64_t)p.C_out / ch / 32 < 65535;   // channel chunks along grid y
+}
+
+bool wg_cl_pointers(const Params &p, const void *x, const void *gy, int ch) {
+    const uintptr_t a = (uintptr_t)(ch * dtype_size(p.dtype));
+    return aligned(x, a) && aligned(gy, a);
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+WgPlan plan_for(const Params &p, bool cl) {
+    WgPlan w{};
+    w.P = (int64_t)p.N * p.OH * p.OW;
+    w.T1 = p.Cin_g * p.KH * p.KW + 1;
+    w.cl = cl;
+    if (cl) {
+        w.tmax = cl_tmax(p);
+        w.ch = cl_ch(p, w.tmax);
+        const int cv = p.C_out / w.ch;
+        w.CVb = cv < 32 ? cv : 32;
+        w.PL = kWgThreads / w.CVb;
+        w.chunks = (int)cdiv(cv, w.CVb);
+        int64_t s = cdiv(kWgBlocksTarget, w.chunks);
+        const int64_t most = cdiv(w.P, (int64_t)w.PL * 4);   // at least ~4 pixels per lane
+        if (s > most) s = most;
+        w.slices = (int)(s < 1 ? 1 : s);
+    } else {
+        int64_t s = cdiv(kWgBlocksTarget, p.C_out > 0 ? p.C_out : 1);
+        const int64_t most = cdiv(w.P, kWgThreads);
+        if (s > most) s = most;
+        w.slices = (int)(s < 1 ? 1 : s);
+    }
+    return w;
+}
+
+// Pixel range [p0, p1) of slice `sl`.
+__device__ __forceinline__ void slice_range(int64_t P, int slices, int sl, int64_t &p0,
+                                            int64_t &p1) {
+    const int64_t per = P / slices, extra = P % slices;
+    p0 = sl * per + (sl < extra ? sl : extra);
+    p1 = p0 + per + (sl < extra ? 1 : 0);
+}
+
+template <typename T, int TMAX, int CH>
+__global__ void __launch_bounds__(kWgThreads)
+wgrad_cl_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__restrict__ ws,
+                Params p, WgPlan pl) {
+    pdl_launch_dependents();
+    pdl_wait();
+    constexpr int PR = CH / 2;                    // channel pairs
+    using V = Vec<T, CH>;
+    using IO = VecIO<CH * (int)sizeof(T)>;
+    __shared__ float red[kWgThreads * CH];        // [pixel lane][block channel]
+
+    const int t = threadIdx.x;
+    const int cvl = t % pl.CVb, lp = t / pl.CVb;
+    const int cv = blockIdx.y * pl.CVb + cvl;
+    const bool active = lp < pl.PL && cv * CH < p.C_out;
+    const int c0 = cv * CH;
+    const int taps = p.KH * p.KW;
+    int64_t p0, p1;
+    slice_range(pl.P, pl.slices, blockIdx.x, p0, p1);
+
+    float2 acc[TMAX][PR];
+    float2 accb[PR];
+#pragma unroll
+    for (int k = 0; k < PR; ++k) accb[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int tp = 0; tp < TMAX; ++tp)
+#pragma unroll
+        for (int k = 0; k < PR; ++k) acc[tp][k] = make_float2(0.f, 0.f);
+
+    if (active) {
+        for (int64_t q = p0 + lp; q < p1; q += pl.PL) {
+            const int ow = (int)(q % p.OW);
+            const int64_t r = q / p.OW;
+            const int oh = (int)(r % p.OH);
+            const int n = (int)(r / p.OH);
+            V gv;
+            IO::load(gv, gy + (int64_t)n * p.ys[0] + (int64_t)oh * p.ys[2] +
+                             (int64_t)ow * p.ys[3] + c0);
+            float2 g2[PR];
+            widen<T, CH>(gv, g2);
+#pragma unroll
+            for (int k = 0; k < PR; ++k) {
+                accb[k].x += g2[k].x;
+                accb[k].y += g2[k].y;
+            }
+            const T *xn = x + (int64_t)n * p.xs[0] + c0;
+#pragma unroll
+            for (int tp = 0; tp < TMAX; ++tp) {
+                if (tp < taps) {
+                    const int kh = tp / p.KW, kw = tp - kh * p.KW;
+                    const int ih = tap_input<false>(oh, kh, p.sh, p.pbh, p.dh, p.H);
+                    const int iw = tap_input<false>(ow, kw, p.sw, p.pbw, p.dw, p.W);
+                    if (ih >= 0 && iw >= 0) {
+                        V xv;
+                        IO::load(xv, xn + (int64_t)ih * p.xs[2] + (int64_t)iw * p.xs[3]);
+                        float2 x2[PR];
+                        widen<T, CH>(xv, x2);
+#pragma unroll
+                        for (int k = 0; k < PR; ++k) fma2_packed(acc[tp][k], g2[k], x2[k]);
+                    }
+                }
+            }
+        }
+    }
+    // Add the pixel lanes, one tap (then the bias) at a time, lanes in order.
+    const int cb = pl.CVb * CH;
+    const int c_first = blockIdx.y * cb;
+#pragma unroll
+    for (int tp = 0; tp <= TMAX; ++tp) {
+        const bool bias_slot = tp == TMAX;
+        if (!bias_slot && tp >= taps) continue;   // the same for the whole block
+        const float2 *src = bias_slot ? accb : acc[bias_slot ? 0 : tp];
+        const int slot = bias_slot ? taps : tp;
+        if (lp < pl.PL) {
+#pragma unroll
+            for (int k = 0; k < PR; ++k) {
+                red[lp * cb + cvl * CH + 2 * k] = src[k].x;
+                red[lp * cb + cvl * CH + 2 * k + 1] = src[k].y;
+            }
+        }
+        __syncthreads();
+        for (int e = t; e < cb; e += blockDim.x) {
+            const int c = c_first + e;
+            if (c < p.C_out) {
+                float s = 0.f;
+                for (int l = 0; l < pl.PL; ++l) s += red[l * cb + e];
+                ws[((int64_t)blockIdx.x * p.C_out + c) * pl.T1 + slot] = s;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWgThreads)
+wgrad_generic_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__restrict__ ws,
+                     Params p, WgPlan pl) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ float warp_sums[kWgThreads / 32];
+    const int t = threadIdx.x;
+    const int khw = p.KH * p.KW;
+    int64_t p0, p1;
+    slice_range(pl.P, pl.slices, blockIdx.x, p0, p1);
+    for (int co = blockIdx.y; co < p.C_out; co += gridDim.y) {
+        const int g = co / p.Cout_g;
+        for (int tap = 0; tap < pl.T1; ++tap) {
+            const bool is_bias = tap == pl.T1 - 1;
+            const int ci = is_bias ? 0 : tap / khw;
+            const int k = is_bias ? 0 : tap - ci * khw;
+            const int kh = k / p.KW, kw = k - kh * p.KW;
+            const T *xc = x + (int64_t)(g * p.Cin_g + ci) * p.xs[1];
+            float s = 0.f;
+            for (int64_t q = p0 + t; q < p1; q += blockDim.x) {
+                const int ow = (int)(q % p.OW);
+                const int64_t r = q / p.OW;
+                const int oh = (int)(r % p.OH);
+                const int n = (int)(r / p.OH);
+                const float gv = load_f32(gy + (int64_t)n * p.ys[0] + (int64_t)co * p.ys[1] +
+                                          (int64_t)oh * p.ys[2] + (int64_t)ow * p.ys[3]);
+                if (is_bias) {
+                    s += gv;
+                } else {
+                    const int ih = tap_input<false>(oh, kh, p.sh, p.pbh, p.dh, p.H);
+                    const int iw = tap_input<false>(ow, kw, p.sw, p.pbw, p.dw, p.W);
+                    if (ih >= 0 && iw >= 0)
+                        s = fmaf(gv, load_f32(xc + (int64_t)n * p.xs[0] + (int64_t)ih * p.xs[2] +
+                                              (int64_t)iw * p.xs[3]),
+                                 s);
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (t % 32 == 0) warp_sums[t / 32] = s;
+            __syncthreads();
+            if (t == 0) {
+                float tot = 0.f;
+                for (int i = 0; i < kWgThreads / 32; ++i) tot += warp_sums[i];
+                ws[((int64_t)blockIdx.x * p.C_out + co) * pl.T1 + tap] = tot;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+wgrad_finish_kernel(const float *__restrict__ ws, T *__restrict__ dw, T *__restrict__ db,
+                    int C_out, int T1, int slices) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t total = (int64_t)C_out * T1;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        double s = 0.0;
+        for (int sl = 0; sl < slices; ++sl) s += (double)ws[(int64_t)sl * total + e];
+        const int co = (int)(e / T1), tap = (int)(e - (int64_t)co * T1);
+        if (tap < T1 - 1)
+            dw[(int64_t)co * (T1 - 1) + tap] = from_f32<T>((float)s);
+        else if (db)
+            db[co] = from_f32<T>((float)s);
+    }
+}
+
+template <typename T, int TMAX>
+cudaError_t launch_cl(const Params &p, const T *x, const T *gy, float *ws, const WgPlan &pl,
+                      cudaStream_t s) {
+    constexpr int CH = wg_ch<T, TMAX>();
+    return launch_pdl(wgrad_cl_kernel<T, TMAX, CH>, dim3(pl.slices, pl.chunks),
+                      dim3(pl.CVb * pl.PL), 0, s, x, gy, ws, p, pl);
+}
+
+}  // namespace
+
+uint64_t wgrad_workspace_bytes(const Params &p) {
+    // Enough for either form, so the size does not depend on the pointers.
+    const WgPlan g = plan_for(p, false);
+    int slices = g.slices;
+    if (cl_shape(p)) {
+        const WgPlan c = plan_for(p, true);
+        if (c.slices > slices) slices = c.slices;
+    }
+    uint64_t b = (uint64_t)slices * (uint64_t)(p.C_out > 0 ? p.C_out : 0) * (uint64_t)g.T1 * 4u;
+    return b < 16 ? 16 : b;
+}
+
+cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *dw, void *db,
+                         void *workspace, cudaStream_t s, int *launches) {
+    *launches = 2;
+    bool cl = cl_shape(p);
+    if (cl) cl = wg_cl_pointers(p, x, gy, cl_ch(p, cl_tmax(p)));
+    const WgPlan pl = plan_for(p, cl);
+    float *ws = static_cast<float *>(workspace);
+    return GCONV_DISPATCH_DTYPE(p.dtype, T, [&] {
+        const T *xt = static_cast<const T *>(x);
+        const T *gt = static_cast<const T *>(gy);
+        cudaError_t e;
+        if (cl) {
+            if (pl.tmax == 9) e = launch_cl<T, 9>(p, xt, gt, ws, pl, s);
+            else if (pl.tmax == 25) e = launch_cl<T, 25>(p, xt, gt, ws, pl, s);
+            else e = launch_cl<T, 49>(p, xt, gt, ws, pl, s);
+        } else {
+            const int gy_blocks = p.C_out < 65535 ? p.C_out : 65535;
+            e = launch_pdl(wgrad_generic_kernel<T>, dim3(pl.slices, gy_blocks), dim3(kWgThreads), 0,
+                           s, xt, gt, ws, p, pl);
+        }
+        if (e != cudaSuccess) return e;
+        const int64_t total = (int64_t)p.C_out * pl.T1;
+        int64_t blocks = (total + 255) / 256;
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        e = launch_pdl(wgrad_finish_kernel<T>, dim3((unsigned)blocks), dim3(256), 0, s,
+                       (const float *)ws, static_cast<T *>(dw), static_cast<T *>(db), p.C_out,
+                       pl.T1, pl.slices);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    });
+}
+
+}  // namespace gconv

@@ -1,8 +1,8 @@
 /*
  * gconv.h -- C ABI of the GB300 direct-stencil convolution library.
  *
- * One operation: 2-D depthwise and few-channel grouped convolution
- * (cross-correlation, zero padding, dilation 1) with
+ * The operation: 2-D depthwise and few-channel grouped convolution
+ * (cross-correlation, zero padding) with
  *   - groups of 1..8 input channels and any number of output channels each
  *     (any depthwise channel multiplier),
  *   - kernels from 1x1 to 9x9 (KH and KW independent), any stride >= 1,
@@ -12,11 +12,23 @@
  *   - NCHW- or channels-last-ordered input, optional bias.
  * The envelope is the one of the direct-stencil template in executorch PR
  * #25085 "Route 2-D depthwise and few-channel grouped convolutions to a
- * Triton direct-stencil kernel" (description, second paragraph).
+ * Triton direct-stencil kernel" (description, second paragraph), which takes
+ * dilation 1 only.  Around it the same library offers, on the same
+ * kernels' designs:
+ *   - dilation >= 1 (taps d apart) and 1-D convolutions (the height-1 case,
+ *     conv1d_bind), the calls executorch PR #25084 says Inductor's templates
+ *     cannot compile (description, first paragraph);
+ *   - the transposed convolution of executorch PR #25091 "Run transposed
+ *     convolutions on the implicit-GEMM template" (description, second
+ *     paragraph; conv_transpose_bind, conv_transpose_forward);
+ *   - the backward of the forward convolution (the gradients that
+ *     torch/_inductor/kernel/conv.py, convolution_backward_lowering,
+ *     lowers: conv_backward_input, conv_backward_weight).
  *
  * Semantics.  For output (n, co, oh, ow), with g = co / Cout_g:
  *   y = b[co] + sum_{ci, kh, kw} w[co, ci, kh, kw] * x[n, g*Cin_g + ci, ih, iw],
- *   ih = oh*stride_h - pad_before_h + kh,  iw = ow*stride_w - pad_before_w + kw,
+ *   ih = oh*stride_h - pad_before_h + kh*dil_h,
+ *   iw = ow*stride_w - pad_before_w + kw*dil_w,
  * where taps with (ih, iw) outside the input contribute zero.  The tap
  * indexing is the one of torch/_inductor/kernel/conv.py, LOOP_BODY_2D; the
  * channel-to-group mapping that of conv2d_template in the same file; the
@@ -29,10 +41,16 @@
  * is allocated once by the caller and the kernels only write into it):
  *   conv_bind -> out_shape_and_stride -> caller allocates y ->
  *   conv_dw_forward (Cin_g == 1) or conv_grouped_forward (1 <= Cin_g <= 8).
+ * Transposed: conv_transpose_bind -> out_shape_and_stride -> allocate y ->
+ *   conv_transpose_forward.
+ * Backward of a forward desc: grad_input_shape_and_stride -> allocate dx ->
+ *   conv_backward_input; conv_backward_weight_workspace_size -> allocate
+ *   the workspace, dw and db -> conv_backward_weight.
  *
- * Ownership.  The caller owns every buffer.  The library allocates no memory
- * (no workspace), keeps no pointer after a call returns and never
- * synchronises; kernels run asynchronously on the caller's stream.
+ * Ownership.  The caller owns every buffer, including the one workspace the
+ * library asks for (conv_backward_weight's).  The library allocates no
+ * memory, keeps no pointer after a call returns and never synchronises;
+ * kernels run asynchronously on the caller's stream.
  *
  * Ordering.  Each forward is one kernel launched with programmatic
  * dependent launch: it may start while the previous kernel on the stream is
@@ -74,19 +92,23 @@ typedef enum gconv_status {
     GCONV_ERR_RANK = 2,          /* x not rank 3/4, w not rank 4, bias not rank 1 */
     GCONV_ERR_DTYPE = 3,         /* unknown dtype code */
     GCONV_ERR_SHAPE = 4,         /* channel/group/weight/bias size mismatch, stride < 1, negative size */
-    GCONV_ERR_UNSUPPORTED = 5,   /* dilation != 1, KH or KW outside [1, 9], Cin_g > 8,
+    GCONV_ERR_UNSUPPORTED = 5,   /* dilation < 1, KH or KW outside [1, 9], Cin_g > 8,
                                     Cin_g != 1 on conv_dw_forward */
     GCONV_ERR_PADDING = 6,       /* negative padding, or the window never fits the padded input */
     GCONV_ERR_ALIGN = 7,         /* a forced schedule needs alignment the pointers lack */
     GCONV_ERR_CUDA = 8,          /* a CUDA launch failed (cudaGetLastError after the launch) */
     GCONV_ERR_INTERNAL = 9,      /* descriptor not produced by conv_bind, or a size overflow */
     GCONV_ERR_LAYOUT = 10,       /* x is neither NCHW- nor channels-last-ordered */
-    GCONV_ERR_SCHEDULE = 11      /* a forced schedule does not support this call */
+    GCONV_ERR_SCHEDULE = 11,     /* a forced schedule does not support this call */
+    GCONV_ERR_KIND = 12,         /* desc of another operation (forward vs transposed) */
+    GCONV_ERR_WORKSPACE = 13     /* workspace missing, too small or misaligned */
 } gconv_status;
 
 /* The five schedules of the direct-stencil template (PR #25085, second
- * paragraph), re-designed for sm_103a.  GCONV_SCHED_AUTO lets the per-shape
- * picker choose. */
+ * paragraph), re-designed for sm_103a, plus a tensor-core schedule for
+ * 4- and 8-channel groups and a channels-last depthwise schedule for the
+ * shapes outside the others' reach (dilated, 1-D, non-square, transposed).
+ * GCONV_SCHED_AUTO lets the per-shape picker choose. */
 typedef enum gconv_schedule {
     GCONV_SCHED_AUTO = -1,
     GCONV_SCHED_DW_FLAT = 0,     /* fallback: any layout, multiplier and group shape */
@@ -101,7 +123,10 @@ typedef enum gconv_schedule {
     GCONV_SCHED_GRP_TC = 5,      /* grouped, 4 or 8 channels per group, channels-last bf16 /
                                     fp16: implicit GEMM on the tcgen05 tensor cores, fp32
                                     accumulation in tensor memory */
-    GCONV_SCHED_COUNT = 6
+    GCONV_SCHED_DW_LINE = 6,     /* channels-last depthwise (multiplier 1), any kernel shape,
+                                    stride and dilation, forward or transposed: a thread per
+                                    16-byte channel vector and strip of output pixels */
+    GCONV_SCHED_COUNT = 7
 } gconv_schedule;
 
 typedef enum gconv_layout {
@@ -119,8 +144,14 @@ typedef struct gconv_tensor {
 } gconv_tensor;
 
 /* The canonical, validated description of one convolution, filled by
- * conv_bind.  Callers may change only `schedule` (GCONV_SCHED_AUTO or a
- * gconv_schedule value to force one schedule for calls with this desc). */
+ * conv_bind (or conv1d_bind, conv_transpose_bind, conv_transpose1d_bind).
+ * Callers may change only `schedule` (GCONV_SCHED_AUTO or a gconv_schedule
+ * value to force one schedule for calls with this desc).
+ * A 1-D convolution is described as the 2-D one of height 1 (H = KH = OH =
+ * 1, stride_h = dil_h = 1, no padding along h); for a transposed one, w is
+ * [C_in, C_out/groups, KH, KW] and w_strides follow that order, H x W is
+ * the input's size and OH x OW the output's, pad_before / pad_after are the
+ * crops before and after, and output_padding extends the end. */
 typedef struct gconv_desc {
     uint32_t magic;              /* set by conv_bind */
     int32_t dtype;               /* gconv_dtype */
@@ -139,7 +170,11 @@ typedef struct gconv_desc {
     int64_t b_stride;            /* elements; 0 when there is no bias */
     int64_t y_strides[4];        /* dense in `layout`, logical (N, C_out, OH, OW) order */
     int32_t x_dense;             /* x is dense (no gaps) in its layout */
+    int32_t transposed;          /* 1: transposed convolution */
+    int32_t spatial_dims;        /* 2, or 1 for conv1d_bind / conv_transpose1d_bind */
     int32_t reserved;
+    int32_t dilation[2];         /* (h, w), >= 1 */
+    int32_t output_padding[2];   /* (h, w), transposed only; 0 otherwise */
 } gconv_desc;
 
 /* Validate the arguments of one convolution and canonicalise them into *out
@@ -150,7 +185,10 @@ typedef struct gconv_desc {
  *   x, w:        required geometries; bias: NULL for no bias.
  *   dtype:       gconv_dtype shared by x, w, bias and y.
  *   stride, padding_before, padding_after, dilation: (h, w) pairs; NULL
- *                stride/dilation mean 1, NULL paddings mean 0.
+ *                stride/dilation mean 1, NULL paddings mean 0.  Dilation d
+ *                spaces the taps d apart, so a window spans d*(K-1)+1 input
+ *                positions and OH = floor((H + pb + pa - d*(KH-1) - 1) /
+ *                stride_h) + 1.
  *   groups:      >= 1, divides C_in and C_out.
  * x must be NCHW-ordered (W stride 1, then H, then C, then N, no overlap) or
  * channels-last-ordered (C stride 1, then W, then H, then N); dims of size 1
@@ -162,6 +200,52 @@ gconv_status conv_bind(const gconv_tensor *x, const gconv_tensor *w,
                        const int32_t padding_after[2], const int32_t dilation[2],
                        int64_t groups, gconv_desc *out);
 
+/* 1-D convolution (PR #25084, first paragraph, names 1-D convolutions among
+ * the calls Inductor's templates cannot compile): x is [N, C_in, L] (or
+ * [C_in, L], one sequence), w [C_out, Cin_g, K], bias [C_out]; stride,
+ * padding and dilation are scalars along L.  x must be NCL-ordered (L
+ * stride 1) or NLC-ordered (channels-last: C stride 1).  The desc is the
+ * height-1 2-D convolution (spatial_dims = 1); out_shape_and_stride gives
+ * [N, C_out, OL] (or [C_out, OL]), dense in x's order, and the forward entry
+ * points run it as they run 2-D calls.  Same errors as conv_bind. */
+gconv_status conv1d_bind(const gconv_tensor *x, const gconv_tensor *w,
+                         const gconv_tensor *bias, int32_t dtype, int32_t stride,
+                         int32_t padding_before, int32_t padding_after,
+                         int32_t dilation, int64_t groups, gconv_desc *out);
+
+/* Transposed 2-D convolution (executorch PR #25091, second paragraph): the
+ * output pixel o reads, at tap k, the input (o + padding_before - k*d) /
+ * stride whenever that is a whole number inside the input, with the weight
+ * w [C_in, C_out/groups, KH, KW] (the forward weight's first two dims
+ * swapped):
+ *   y[n, co, oh, ow] = b[co] + sum_{ci, kh, kw} w[g*Cin_g + ci, co - g*Cout_g, kh, kw]
+ *                               * x[n, g*Cin_g + ci, ih, iw],
+ *   ih = (oh + pad_before_h - kh*dil_h) / stride_h (a whole number in [0, H)),
+ *   iw likewise.
+ * OH = (H - 1)*stride_h + dil_h*(KH - 1) + 1 + output_padding_h
+ *      - padding_before_h - padding_after_h  (the uncropped output, extended
+ * by output_padding at the end, cropped by the two paddings -- asymmetric
+ * crops allowed); OH < 1 is GCONV_ERR_PADDING.  0 <= output_padding.
+ * Envelope: KH, KW in [1, 9], Cin_g = C_in/groups <= 8 (the direct-stencil
+ * bound, read on the transposed input side), any stride and dilation.
+ * x layout, unbatched rank-3 input and the output layout follow conv_bind.
+ * Run it with conv_transpose_forward. */
+gconv_status conv_transpose_bind(const gconv_tensor *x, const gconv_tensor *w,
+                                 const gconv_tensor *bias, int32_t dtype,
+                                 const int32_t stride[2], const int32_t padding_before[2],
+                                 const int32_t padding_after[2],
+                                 const int32_t output_padding[2], const int32_t dilation[2],
+                                 int64_t groups, gconv_desc *out);
+
+/* Transposed 1-D convolution: x [N, C_in, L] (or [C_in, L]), w [C_in,
+ * C_out/groups, K]; the height-1 case of conv_transpose_bind (PR #25091's
+ * benchmark adds 1-D transposed upsampling, kernel 4 stride 2). */
+gconv_status conv_transpose1d_bind(const gconv_tensor *x, const gconv_tensor *w,
+                                   const gconv_tensor *bias, int32_t dtype,
+                                   int32_t stride, int32_t padding_before,
+                                   int32_t padding_after, int32_t output_padding,
+                                   int32_t dilation, int64_t groups, gconv_desc *out);
+
 /* The output's rank, sizes and element strides (PR #25084, second paragraph:
  * one function decides the output layout and both the op and its shape-only
  * variant use it).  OH = floor((H + pad_before_h + pad_after_h - KH) /
@@ -171,7 +255,9 @@ gconv_status conv_bind(const gconv_tensor *x, const gconv_tensor *w,
 gconv_status out_shape_and_stride(const gconv_desc *d, int32_t *rank,
                                   int64_t sizes[4], int64_t strides[4]);
 
-/* Depthwise forward (Cin_g == 1, any multiplier C_out / C_in).  x, w, bias
+/* Depthwise forward (Cin_g == 1, any multiplier C_out / C_in).  Takes a
+ * forward desc (conv_bind or conv1d_bind); a transposed one is
+ * GCONV_ERR_KIND.  x, w, bias
  * and y are device pointers laid out as the geometries given to conv_bind
  * and as out_shape_and_stride says for y; bias must be NULL exactly when the
  * desc has none.  Launches on `stream` and returns without waiting.  Empty
@@ -186,6 +272,17 @@ gconv_status conv_grouped_forward(const gconv_desc *d, const void *x,
                                   const void *w, const void *bias, void *y,
                                   gconv_stream stream);
 
+/* Transposed forward: runs a desc from conv_transpose_bind or
+ * conv_transpose1d_bind (a forward desc is GCONV_ERR_KIND).  Pointers,
+ * stream and errors as conv_dw_forward; w is [C_in, C_out/groups, KH, KW]
+ * by the strides given to the bind.  A stride-1 transposed convolution
+ * with one input channel per group is the forward convolution with the
+ * kernel flipped and padding d*(K-1) - crop, and runs on the forward
+ * schedules; the others run on dw_line (channels-last depthwise), or
+ * grp_reduce / dw_flat. */
+gconv_status conv_transpose_forward(const gconv_desc *d, const void *x, const void *w,
+                                    const void *bias, void *y, gconv_stream stream);
+
 /* Which schedule a forward call with this desc and these pointers would run
  * (the picker, or the forced schedule), without launching anything.  Pointer
  * values are only inspected for alignment.  Returns GCONV_ERR_SCHEDULE /
@@ -193,6 +290,45 @@ gconv_status conv_grouped_forward(const gconv_desc *d, const void *x,
 gconv_status conv_select_schedule(const gconv_desc *d, const void *x,
                                   const void *w, const void *bias,
                                   const void *y, int32_t *schedule);
+
+/* ---------------------------------------------------------------- backward
+ * The gradients of the forward convolution described by a forward desc d
+ * (torch/_inductor/kernel/conv.py, convolution_backward_lowering: grad
+ * input, grad weight, and grad bias = the sum of grad_output over batch and
+ * space).  gy, the output gradient, has the sizes and strides that
+ * out_shape_and_stride gives for y. */
+
+/* Sizes and strides of dx: x's sizes, dense in x's layout (NCHW or
+ * channels-last; rank 3 / 2 for unbatched or 1-D descs, as x was). */
+gconv_status grad_input_shape_and_stride(const gconv_desc *d, int32_t *rank,
+                                         int64_t sizes[4], int64_t strides[4]);
+
+/* dx = the gradient of sum(y * gy) with respect to x: every forward product
+ * w * x sends gy * w to dx at x's index.  It is the transposed convolution
+ * of gy with the forward weight (same stride, dilation and groups, crop
+ * pad_before, sized back to H x W), and runs on the transposed schedules.
+ * gy, w, dx are device pointers (dx laid out as grad_input_shape_and_stride
+ * says); fp32 accumulation, one rounding to the dtype.  Same stream and error
+ * contract as the forward. */
+gconv_status conv_backward_input(const gconv_desc *d, const void *gy, const void *w,
+                                 void *dx, gconv_stream stream);
+
+/* Bytes of device workspace conv_backward_weight needs for this desc (the
+ * fp32 partial sums of its first pass).  Pure host code. */
+gconv_status conv_backward_weight_workspace_size(const gconv_desc *d, uint64_t *bytes);
+
+/* dw[co, ci, kh, kw] = sum over n, oh, ow of gy[n, co, oh, ow] * x[n, g*Cin_g + ci, ih, iw]
+ * (the taps of the forward), written dense [C_out, Cin_g, KH, KW] in the
+ * dtype; db[co] = sum over n, oh, ow of gy[n, co, oh, ow], dense [C_out]
+ * (db may be NULL to skip it).  Two launches: partial sums over slices of
+ * the output pixels in fp32 into `workspace` (at least the bytes
+ * conv_backward_weight_workspace_size gives, 16-byte aligned, owned by the
+ * caller and not read before it is written), then a pass that adds the
+ * slices in fp64 in a fixed order and rounds once.  The result is
+ * deterministic.  x and gy as for the forward and conv_backward_input. */
+gconv_status conv_backward_weight(const gconv_desc *d, const void *x, const void *gy,
+                                  void *dw, void *db, void *workspace,
+                                  uint64_t workspace_bytes, gconv_stream stream);
 
 /* Process-wide override for tests (the force_conv_candidate hook of PR
  * #25084): every later call whose desc has schedule == GCONV_SCHED_AUTO runs

@@ -321,3 +321,23 @@ def violations(got, ref, bound, dtype: str):
     with np.errstate(invalid="ignore"):
         bad = ~(np.abs(got - ref) <= tol * bound + ABS_TOL)
     return bad
+
+
+def reference(wl, x, w, b=None):
+    """The oracle function that a workload description names (duck-typed:
+    stride, pad_before, pad_after, groups, dilation, transposed,
+    output_padding, spatial_dims attributes; 1-D workloads use the second
+    element of each pair).  Returns (y, bound)."""
+    dil = getattr(wl, "dilation", (1, 1))
+    tr = getattr(wl, "transposed", False)
+    op = getattr(wl, "output_padding", (0, 0))
+    if getattr(wl, "spatial_dims", 2) == 1:
+        if tr:
+            return conv_transpose1d(x, w, b, wl.stride[1], wl.pad_before[1], wl.pad_after[1],
+                                    op[1], wl.groups, dil[1])
+        return conv1d(x, w, b, wl.stride[1], wl.pad_before[1], wl.pad_after[1], wl.groups,
+                      dil[1])
+    if tr:
+        return conv_transpose2d(x, w, b, wl.stride, wl.pad_before, wl.pad_after, op,
+                                wl.groups, dil)
+    return conv2d(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.groups, dil)

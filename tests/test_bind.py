@@ -13,7 +13,8 @@ import oracle
 from grouped_convolution_gb300.inputs import WORKLOADS
 
 ERR = {"NULL": 1, "RANK": 2, "DTYPE": 3, "SHAPE": 4, "UNSUPPORTED": 5, "PADDING": 6,
-       "ALIGN": 7, "CUDA": 8, "INTERNAL": 9, "LAYOUT": 10, "SCHEDULE": 11}
+       "ALIGN": 7, "CUDA": 8, "INTERNAL": 9, "LAYOUT": 10, "SCHEDULE": 11, "KIND": 12,
+       "WORKSPACE": 13}
 
 FAKE = 1 << 20   # a 1 MiB-aligned fake device address; never dereferenced
 
@@ -72,7 +73,8 @@ def test_valid_depthwise_desc():
     (dict(b=((5,), None)), "SHAPE"),                         # bias size
     (dict(stride=0), "SHAPE"),
     (dict(groups=0), "SHAPE"),
-    (dict(dil=2), "UNSUPPORTED"),
+    (dict(dil=0), "UNSUPPORTED"),
+    (dict(dil=4, pb=0, pa=0), "PADDING"),                    # dilated span 9 > 8
     (dict(w=((4, 1, 10, 3), None)), "UNSUPPORTED"),          # KH > 9
     (dict(w=((4, 1, 3, 10), None)), "UNSUPPORTED"),          # KW > 9
     (dict(x=((1, 9, 8, 8), None), w=((9, 9, 3, 3), None), groups=1), "UNSUPPORTED"),  # Cin_g 9

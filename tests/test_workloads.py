@@ -20,8 +20,15 @@ pytestmark = pytest.mark.gpu
 
 def gpu_conv(wl, x, w, b, schedule=None):
     dev = torch.device("cuda")
-    return gc.conv2d(x.to(dev), w.to(dev), b.to(dev) if b is not None else None,
-                     wl.stride, wl.pad_before, wl.pad_after, wl.groups, schedule=schedule)
+    xd, wd = x.to(dev), w.to(dev)
+    bd = b.to(dev) if b is not None else None
+    d = gc.bind(xd, wd, bd, wl.stride, wl.pad_before, wl.pad_after, wl.dilation, wl.groups,
+                wl.transposed, wl.output_padding)
+    if schedule is not None:
+        d.schedule = gc.SCHEDULES[schedule]
+    y = gc.empty_output(d, xd)
+    gc.run(d, xd, wd, bd, y)
+    return y
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
@@ -30,7 +37,7 @@ def test_full_size_workload(name):
     x, w, b = make_inputs(wl)
     y = gpu_conv(wl, x, w, b)
     torch.cuda.synchronize()
-    ref, bound = oracle.conv2d(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.groups)
+    ref, bound = oracle.reference(wl, x, w, b)
     got = y.cpu()
     assert tuple(got.shape) == ref.shape
     bad = oracle.violations(got, ref, bound, wl.dtype)
@@ -41,7 +48,8 @@ def test_full_size_workload(name):
     assert float(np.max(err / (bound + np.abs(ref) + 1e-30))) < 64 * eps
 
 
-@pytest.mark.parametrize("schedule", ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc"])
+@pytest.mark.parametrize("schedule", ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce",
+                                      "grp_tc", "dw_line"])
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_reduced_workload_every_schedule(name, schedule):
     wl = small_variant(WORKLOADS[name], N=2, H=min(WORKLOADS[name].H, 29),
@@ -54,6 +62,6 @@ def test_reduced_workload_every_schedule(name, schedule):
             pytest.skip(f"{schedule} does not take {name}")
         raise
     torch.cuda.synchronize()
-    ref, bound = oracle.conv2d(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.groups)
+    ref, bound = oracle.reference(wl, x, w, b)
     bad = oracle.violations(y.cpu(), ref, bound, wl.dtype)
     assert not bad.any(), f"{int(bad.sum())} of {bad.size} outside tolerance"
