@@ -30,7 +30,8 @@ __all__ = [
     "conv_schedule_name", "conv_strerror", "conv_launch_count", "conv2d",
     "conv1d_bind", "conv_transpose_bind", "conv_transpose1d_bind", "conv_transpose_forward",
     "grad_input_shape_and_stride", "conv_backward_input", "conv_backward_weight_workspace_size",
-    "conv_backward_weight", "conv1d", "conv_transpose2d", "conv_transpose1d",
+    "conv_backward_weight", "conv_backward_weight_noalloc", "conv_backward_weight_noalloc_limit",
+    "conv1d", "conv_transpose2d", "conv_transpose1d",
     "conv2d_backward", "GconvError", "SCHEDULES", "lib_path",
 ]
 
@@ -119,6 +120,10 @@ def _load():
         lib.conv_backward_weight_workspace_size.argtypes = [P(Desc), P(ctypes.c_uint64)]
         lib.conv_backward_weight.restype = i32
         lib.conv_backward_weight.argtypes = [P(Desc), vp, vp, vp, vp, vp, ctypes.c_uint64, vp]
+        lib.conv_backward_weight_noalloc.restype = i32
+        lib.conv_backward_weight_noalloc.argtypes = [P(Desc), vp, vp, vp, vp, vp]
+        lib.conv_backward_weight_noalloc_limit.restype = ctypes.c_uint64
+        lib.conv_backward_weight_noalloc_limit.argtypes = []
         lib.conv_select_schedule.restype = i32
         lib.conv_select_schedule.argtypes = [P(Desc), vp, vp, vp, vp, P(i32)]
         lib.conv_force_schedule.restype = i32
@@ -347,6 +352,20 @@ def conv_backward_weight(desc: Desc, x, gy, dw, db, workspace, workspace_bytes=N
     _check(_load().conv_backward_weight(ctypes.byref(desc), _ptr(x), _ptr(gy), _ptr(dw),
                                         _ptr(db), _ptr(workspace), int(workspace_bytes),
                                         _stream_ptr(stream)), "conv_backward_weight")
+
+
+def conv_backward_weight_noalloc(desc: Desc, x, gy, dw, db, stream=None):
+    """conv_backward_weight with the library's fixed device scratch buffer
+    instead of a caller workspace, for callers that cannot allocate device
+    memory (see include/gconv.h)."""
+    _check(_load().conv_backward_weight_noalloc(ctypes.byref(desc), _ptr(x), _ptr(gy),
+                                                _ptr(dw), _ptr(db), _stream_ptr(stream)),
+           "conv_backward_weight_noalloc")
+
+
+def conv_backward_weight_noalloc_limit() -> int:
+    """Bytes of the fixed scratch buffer conv_backward_weight_noalloc uses."""
+    return int(_load().conv_backward_weight_noalloc_limit())
 
 
 def conv_select_schedule(desc: Desc, x, w, bias, y) -> str:

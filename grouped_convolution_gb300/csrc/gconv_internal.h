@@ -57,6 +57,11 @@ inline bool plain_forward(const gconv_desc &d) {
     return !d.transposed && d.dilation[0] == 1 && d.dilation[1] == 1;
 }
 
+// Bookkeeping shared by entry points outside host.cpp: the launch counter
+// behind conv_launch_count and the error behind conv_last_cuda_error.
+void note_launches(int launches);
+void note_cuda_error(int32_t e);
+
 // Backward weight pass (k_wgrad.cu): workspace bytes, and the launches.
 uint64_t wgrad_workspace_bytes(const Params &p);
 cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *dw, void *db,

@@ -111,6 +111,12 @@ bool ordered(const int64_t sizes[4], const int64_t strides[4], const int order[4
 
 namespace gconv {
 
+void note_launches(int launches) {
+    g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
+}
+
+void note_cuda_error(int32_t e) { t_last_cuda_error = e; }
+
 Params make_params(const gconv_desc &d) {
     Params p{};
     p.N = (int)d.N; p.C_in = (int)d.C_in; p.H = (int)d.H; p.W = (int)d.W;
@@ -671,6 +677,7 @@ const char *conv_strerror(gconv_status s) {
     case GCONV_ERR_SCHEDULE: return "forced schedule does not support this convolution";
     case GCONV_ERR_KIND: return "descriptor of another operation (forward vs transposed)";
     case GCONV_ERR_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
+    case GCONV_ERR_SCRATCH_LIMIT: return "needs more scratch than the library's fixed device buffer holds";
     }
     return "unknown status";
 }

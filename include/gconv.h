@@ -101,7 +101,9 @@ typedef enum gconv_status {
     GCONV_ERR_LAYOUT = 10,       /* x is neither NCHW- nor channels-last-ordered */
     GCONV_ERR_SCHEDULE = 11,     /* a forced schedule does not support this call */
     GCONV_ERR_KIND = 12,         /* desc of another operation (forward vs transposed) */
-    GCONV_ERR_WORKSPACE = 13     /* workspace missing, too small or misaligned */
+    GCONV_ERR_WORKSPACE = 13,    /* workspace missing, too small or misaligned */
+    GCONV_ERR_SCRATCH_LIMIT = 14 /* conv_backward_weight_noalloc: the problem needs more
+                                    scratch than its fixed device buffer holds */
 } gconv_status;
 
 /* The five schedules of the direct-stencil template (PR #25085, second
@@ -329,6 +331,28 @@ gconv_status conv_backward_weight_workspace_size(const gconv_desc *d, uint64_t *
 gconv_status conv_backward_weight(const gconv_desc *d, const void *x, const void *gy,
                                   void *dw, void *db, void *workspace,
                                   uint64_t workspace_bytes, gconv_stream stream);
+
+/* conv_backward_weight without a caller workspace, for callers that cannot
+ * allocate device memory: code inside a host framework that owns every
+ * device allocation (only its pool may be used, and this library has no
+ * handle to it), or code on a fixed memory budget that allows no allocation
+ * after start-up.  The pages have no counterpart; the computation and the
+ * result are those of conv_backward_weight (same kernels, bit for bit).
+ * Its scratch is a fixed buffer of conv_backward_weight_noalloc_limit()
+ * bytes (8 MiB) in device memory, which every GPU that loads the library
+ * holds until the process exits; a problem whose
+ * conv_backward_weight_workspace_size exceeds it gets
+ * GCONV_ERR_SCRATCH_LIMIT.  The first call with a device current looks the
+ * buffer's address up on that device (make it before any stream capture
+ * begins).  The call itself allocates nothing.  All calls share the buffer:
+ * each writes every scratch entry before reading it, so no clearing is
+ * needed, but calls whose kernels overlap on the GPU race on it -- keep
+ * them ordered on one stream. */
+gconv_status conv_backward_weight_noalloc(const gconv_desc *d, const void *x, const void *gy,
+                                          void *dw, void *db, gconv_stream stream);
+
+/* Size in bytes of conv_backward_weight_noalloc's fixed device buffer. */
+uint64_t conv_backward_weight_noalloc_limit(void);
 
 /* Process-wide override for tests (the force_conv_candidate hook of PR
  * #25084): every later call whose desc has schedule == GCONV_SCHED_AUTO runs
