@@ -58,11 +58,21 @@ def parse():
 
 
 def run_case(args):
-    """Run one workload a few times through the C ABI, for ncu captures."""
+    """Run one workload a few times through the C ABI, for ncu captures.
+    ``<workload>.backward_input`` / ``.backward_weight`` run that backward
+    pass instead."""
     import torch
     import grouped_convolution_gb300 as gc
     from grouped_convolution_gb300.inputs import WORKLOADS, make_inputs
     gc.build()
+    if ".backward_" in args.case:
+        base, part = args.case.split(".backward_")
+        c = BackwardCase(base, 1, "cuda", part)
+        for i in range(args.reps):
+            c.run(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": args.case, "reps": args.reps}))
+        return
     wl = WORKLOADS[args.case]
     x, w, b = make_inputs(wl, device="cuda")
     d = gc.bind(x, w, b, wl.stride, wl.pad_before, wl.pad_after, wl.dilation, wl.groups,

@@ -55,6 +55,36 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half *) {
 template <typename T>
 __device__ __forceinline__ float load_f32(const T *p) { return Elem<T>::load(p); }
 
+// Division of 32-bit unsigned n by a divisor d fixed for a launch, by a
+// multiply-high and shifts (T. Granlund and P. L. Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, section 4: with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// q = (t + ((n - t) >> 1)) >> (l - 1) where t = mulhi(m, n), for l >= 1;
+// q = n for d = 1).  A runtime integer division costs tens of
+// instructions; this costs four.  Built on the host, used on the device.
+struct FastDiv {
+    uint32_t d, m, l;
+    FastDiv() : d(1), m(0), l(0) {}
+    explicit FastDiv(uint32_t dd) : d(dd ? dd : 1), m(0), l(0) {
+        while ((1ull << l) < d) ++l;
+        if (l > 0) m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+    }
+    __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        if (l == 0) return n;
+#ifdef __CUDA_ARCH__
+        const uint32_t t = __umulhi(m, n);
+#else
+        const uint32_t t = (uint32_t)(((uint64_t)m * n) >> 32);
+#endif
+        return (t + ((n - t) >> 1)) >> (l - 1);
+    }
+    // n = q*d + r
+    __host__ __device__ __forceinline__ void divmod(uint32_t n, uint32_t &q, uint32_t &r) const {
+        q = div(n);
+        r = n - q * d;
+    }
+};
+
 // The input index that output index o reads at tap k along one dim, or -1
 // when the tap falls outside the input.  Forward: o*s - pb + k*d (the conv.py
 // LOOP_BODY_2D rule with dilation).  Transposed (executorch PR #25091,

@@ -11,10 +11,24 @@
 // row (grid-stride over blockIdx.x).  Lane (cv, strip): cv fastest, so the
 // lanes of a warp read and write consecutive 16-byte vectors of one pixel
 // (fully used 32-byte sectors).  The chunk's KH*KW weights and its bias sit
-// in shared memory as fp32 [tap][channel] and are read as broadcast vectors;
-// input vectors are read straight from global memory (the other taps' reads
-// of a pixel hit L1), widened once per read, and multiplied into fp32
-// accumulators with packed FMAs; one rounding per output at the store.
+// in shared memory as fp32 [tap][channel] and are read as broadcast vectors.
+// For each kernel row, a lane first issues the loads of all KW x S input
+// vectors it needs (taps outside the input are skipped), so they are in
+// flight together -- the other taps' reads of a pixel hit L1, and with one
+// load at a time a lane would wait a full memory latency per tap -- then
+// widens each and multiplies it into fp32 accumulators with packed FMAs;
+// one rounding per output at the store.  The kernel width bound KWM (4 or
+// 9) is a template parameter so the load slots are registers; S = 4 pixels
+// per lane for KWM = 4, 2 for KWM = 9.  Blocks are persistent (as many as
+// fit at once), so the weights are staged once per block.
+// Transposed calls walk strips of one column phase: outputs q*s + ph for S
+// consecutive q all read tap k at input q + c(ph, k) (c from a per-block
+// table of (phase, tap) offsets, none when that phase skips the tap), so a
+// strip needs no division and reads consecutive inputs; the output row's
+// taps come from a second table the same way.
+// Forward calls with stride 1 and dilation 1 keep a register sliding window
+// instead: the S + KW - 1 input vectors of a strip's row are loaded and
+// widened once, and every tap reads its S vectors from the window.
 #include "device_common.cuh"
 #include "gconv_internal.h"
 #include "launch.cuh"
@@ -23,8 +37,12 @@
 namespace gconv {
 namespace {
 
-constexpr int kLineThreads = 256;
-constexpr int kLineS = 4;   // output pixels per lane
+// 128-thread blocks: a lane holds ~160 registers (its loads in flight), so
+// smaller blocks let three of them share an SM.
+constexpr int kLineThreads = 128;
+// Output pixels per lane for kernel widths up to KWM.
+constexpr int line_s(int KWM) { return KWM <= 4 ? 4 : 2; }
+constexpr int line_kwm(int KW) { return KW <= 4 ? 4 : 9; }
 
 template <typename T> constexpr int line_vec() { return 16 / (int)sizeof(T); }
 
@@ -32,22 +50,57 @@ struct LineGeom {
     int CV;      // channel vectors in the tensor
     int CVb;     // channel vectors per block (lanes along channels)
     int PB;      // strips per block pass (lanes along pixels)
-    int NSW;     // strips per output row
-    int64_t items;   // N * OH * NSW
+    int NSW;     // strips per output row (per column phase when transposed)
+    int64_t items;   // N * OH * NSW (* stride_w when transposed), < 2^31
+    int tab_w, tab_h;   // transposed: offsets of the column / row tap tables (ints)
+    FastDiv fd_nsw, fd_sw, fd_oh, fd_sh;   // item decomposition without divisions
 };
+
+// Tap tables of a transposed call (entries per phase x tap) must fit here.
+constexpr int kLineTabMax = 2048;
 
 bool line_geometry(const Params &p, int es, LineGeom &g) {
     const int vec = 16 / es;
     if (p.C_out % vec != 0) return false;
+    const int S = line_s(line_kwm(p.KW));
     g.CV = p.C_out / vec;
-    g.CVb = g.CV < 32 ? g.CV : 32;
+    const int chunks = (g.CV + 31) / 32;         // balanced chunks of <= 32 vectors
+    g.CVb = (g.CV + chunks - 1) / chunks;
     g.PB = kLineThreads / g.CVb;
-    g.NSW = (p.OW + kLineS - 1) / kLineS;
-    g.items = (int64_t)p.N * p.OH * g.NSW;
-    return g.CV >= 1;
+    if (p.transposed) {
+        // Strips of one column phase ph: outputs q*sw + ph for S consecutive q.
+        const int Q = (p.OW + p.sw - 1) / p.sw;
+        g.NSW = (Q + S - 1) / S;
+        g.items = (int64_t)p.N * p.OH * p.sw * g.NSW;
+        if ((int64_t)p.sw * p.KW > kLineTabMax || (int64_t)p.sh * p.KH > kLineTabMax) return false;
+    } else {
+        g.NSW = (p.OW + S - 1) / S;
+        g.items = (int64_t)p.N * p.OH * g.NSW;
+    }
+    const int cb = g.CVb * vec;
+    g.tab_w = (p.KH * p.KW + 1) * cb;            // after the fp32 weights (same 4-byte units)
+    g.tab_h = g.tab_w + (p.transposed ? p.sw * p.KW : 0);
+    g.fd_nsw = FastDiv((uint32_t)g.NSW);
+    g.fd_sw = FastDiv((uint32_t)p.sw);
+    g.fd_oh = FastDiv((uint32_t)p.OH);
+    g.fd_sh = FastDiv((uint32_t)p.sh);
+    return g.CV >= 1 && g.items <= INT32_MAX;
 }
 
-template <typename T, bool TR>
+size_t line_smem(const Params &p, const LineGeom &g) {
+    return (size_t)(g.tab_h + (p.transposed ? p.sh * p.KH : 0)) * 4;
+}
+
+// Transposed tap table entry: for phase r (0 <= r < s) and tap k, the
+// offset c with input = (o - r) / s + c for every output o = r (mod s), or
+// kNoTap when no output of that phase reads tap k.
+constexpr int kNoTap = -0x40000000;
+__device__ __forceinline__ int tr_offset(int r, int k, int s, int pb, int d) {
+    const int num = r + pb - k * d;
+    return (num % s == 0) ? num / s : kNoTap;
+}
+
+template <typename T, bool TR, int KWM, bool UNIT>
 __global__ void __launch_bounds__(kLineThreads)
 line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
             T *__restrict__ y, Params p, LineGeom g) {
@@ -57,10 +110,14 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
     pdl_wait();
     constexpr int VEC = line_vec<T>();
     constexpr int P = VEC / 2;
-    constexpr int S = kLineS;
+    constexpr int S = line_s(KWM);
     using V = Vec<T, VEC>;
     using IO = VecIO<16>;
-    extern __shared__ __align__(16) float line_w[];   // [KH*KW + 1][CVb * VEC]
+    // [KH*KW + 1][CVb * VEC] fp32 weights and bias, then (transposed) the
+    // column and row tap tables.
+    extern __shared__ __align__(16) float line_w[];
+    int *tab_w = reinterpret_cast<int *>(line_w) + g.tab_w;
+    int *tab_h = reinterpret_cast<int *>(line_w) + g.tab_h;
 
     const int taps = p.KH * p.KW;
     const int cb = g.CVb * VEC;                  // channels per block
@@ -82,6 +139,12 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
         }
         line_w[e] = v;
     }
+    if constexpr (TR) {
+        for (int e = t; e < p.sw * p.KW; e += blockDim.x)
+            tab_w[e] = tr_offset(e / p.KW, e % p.KW, p.sw, p.pbw, p.dw);
+        for (int e = t; e < p.sh * p.KH; e += blockDim.x)
+            tab_h[e] = tr_offset(e / p.KH, e % p.KH, p.sh, p.pbh, p.dh);
+    }
     __syncthreads();
 
     const int cvl = t % g.CVb, lane_strip = t / g.CVb;
@@ -94,36 +157,119 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
 #pragma unroll
     for (int k = 0; k < P; ++k) bias[k] = wv[(taps * cb) / 2 + k];
 
-    for (int64_t item = (int64_t)blockIdx.x * g.PB + lane_strip; item < g.items;
-         item += (int64_t)gridDim.x * g.PB) {
-        const int sx = (int)(item % g.NSW);
-        const int64_t r = item / g.NSW;
-        const int oh = (int)(r % p.OH);
-        const int n = (int)(r / p.OH);
-        const int ow0 = sx * S;
+    const uint32_t items = (uint32_t)g.items;
+    for (uint32_t item = blockIdx.x * g.PB + lane_strip; item < items;
+         item += gridDim.x * g.PB) {
+        // Output pixel i of the strip is column ow0 + i*ostep.
+        uint32_t r, sxu;
+        g.fd_nsw.divmod(item, r, sxu);
+        const int sx = (int)sxu;
+        int ph = 0;
+        if constexpr (TR) {
+            uint32_t r2, phu;
+            g.fd_sw.divmod(r, r2, phu);
+            ph = (int)phu;
+            r = r2;
+        }
+        uint32_t nu, ohu;
+        g.fd_oh.divmod(r, nu, ohu);
+        const int oh = (int)ohu;
+        const int n = (int)nu;
+        const int ostep = TR ? p.sw : 1;
+        const int q0 = sx * S;                   // transposed: first q of the strip
+        const int ow0 = TR ? q0 * p.sw + ph : q0;
         float2 acc[S][P];
 #pragma unroll
         for (int i = 0; i < S; ++i)
 #pragma unroll
             for (int k = 0; k < P; ++k) acc[i][k] = bias[k];
         const T *xn = x + (int64_t)n * p.xs[0] + c0;
+        int qh = 0, rh = 0;
+        if constexpr (TR) {
+            uint32_t qhu, rhu;
+            g.fd_sh.divmod((uint32_t)oh, qhu, rhu);
+            qh = (int)qhu;
+            rh = (int)rhu;
+        }
         for (int kh = 0; kh < p.KH; ++kh) {
-            const int ih = tap_input<TR>(oh, kh, p.sh, p.pbh, p.dh, p.H);
+            int ih;
+            if constexpr (TR) {
+                const int c = tab_h[rh * p.KH + kh];
+                ih = c == kNoTap ? -1 : qh + c;
+                if (ih >= p.H) ih = -1;
+            } else {
+                ih = oh * p.sh - p.pbh + kh * p.dh;
+                if (ih >= p.H) ih = -1;
+            }
             if (ih < 0) continue;
             const T *xr = xn + (int64_t)ih * p.xs[2];
-            for (int kw = 0; kw < p.KW; ++kw) {
+            if constexpr (UNIT) {
+                // Stride 1, dilation 1: the strip's S + KW - 1 input vectors
+                // form one window; each is loaded and widened once and
+                // slides under the taps.
+                constexpr int NW = S + KWM - 1;
+                float2 win[NW][P];
+                const int iw0 = ow0 - p.pbw;
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    const int iw = iw0 + j;
+                    if (j < S + p.KW - 1 && iw >= 0 && iw < p.W) {
+                        V v;
+                        IO::load(v, xr + (int64_t)iw * p.xs[3]);
+                        widen<T, VEC>(v, win[j]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < P; ++k) win[j][k] = make_float2(0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int kw = 0; kw < KWM; ++kw) {
+                    if (kw >= p.KW) break;
+                    float2 wk[P];
+                    const float2 *src = wv + ((kh * p.KW + kw) * cb) / 2;
+#pragma unroll
+                    for (int k = 0; k < P; ++k) wk[k] = src[k];
+#pragma unroll
+                    for (int i = 0; i < S; ++i)
+#pragma unroll
+                        for (int k = 0; k < P; ++k) fma2_packed(acc[i][k], wk[k], win[i + kw][k]);
+                }
+                continue;
+            }
+            // Every load of this kernel row first ...
+            V raw[KWM][S];
+            bool ok[KWM][S];
+#pragma unroll
+            for (int kw = 0; kw < KWM; ++kw) {
+                int base;                        // input column of pixel 0 at tap kw
+                bool tap_ok = kw < p.KW;
+                if constexpr (TR) {
+                    const int c = tap_ok ? tab_w[ph * p.KW + kw] : kNoTap;
+                    tap_ok = c != kNoTap;
+                    base = q0 + c;
+                } else {
+                    base = ow0 * p.sw - p.pbw + kw * p.dw;
+                }
+#pragma unroll
+                for (int i = 0; i < S; ++i) {
+                    const int iw = base + i * (TR ? 1 : p.sw);
+                    ok[kw][i] = tap_ok && iw >= 0 && iw < p.W && ow0 + i * ostep < p.OW;
+                    if (ok[kw][i]) IO::load(raw[kw][i], xr + (int64_t)iw * p.xs[3]);
+                }
+            }
+            // ... then the arithmetic.
+#pragma unroll
+            for (int kw = 0; kw < KWM; ++kw) {
+                if (kw >= p.KW) break;
                 float2 wk[P];
                 const float2 *src = wv + ((kh * p.KW + kw) * cb) / 2;
 #pragma unroll
                 for (int k = 0; k < P; ++k) wk[k] = src[k];
 #pragma unroll
                 for (int i = 0; i < S; ++i) {
-                    const int iw = tap_input<TR>(ow0 + i, kw, p.sw, p.pbw, p.dw, p.W);
-                    if (iw < 0 || ow0 + i >= p.OW) continue;
-                    V v;
-                    IO::load(v, xr + (int64_t)iw * p.xs[3]);
+                    if (!ok[kw][i]) continue;
                     float2 xf[P];
-                    widen<T, VEC>(v, xf);
+                    widen<T, VEC>(raw[kw][i], xf);
 #pragma unroll
                     for (int k = 0; k < P; ++k) fma2_packed(acc[i][k], wk[k], xf[k]);
                 }
@@ -132,7 +278,8 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
         T *yp = y + (int64_t)n * p.ys[0] + (int64_t)oh * p.ys[2] + (int64_t)ow0 * p.ys[3] + c0;
 #pragma unroll
         for (int i = 0; i < S; ++i)
-            if (ow0 + i < p.OW) IO::store(yp + (int64_t)i * p.ys[3], pack_pairs<T, VEC>(acc[i]));
+            if (ow0 + i * ostep < p.OW)
+                IO::store(yp + (int64_t)i * ostep * p.ys[3], pack_pairs<T, VEC>(acc[i]));
     }
 }
 
@@ -150,12 +297,12 @@ bool line_supports(const gconv_desc &d, const Ptrs &q) {
     if (d.y_strides[1] != 1 || d.y_strides[3] % vec || d.y_strides[2] % vec ||
         d.y_strides[0] % vec)
         return false;
-    // weights and bias staged in shared memory
-    const size_t smem = (size_t)(d.KH * d.KW + 1) * 32 * vec * sizeof(float);
-    if (smem > 200 * 1024) return false;
     Params p = make_params(d);
     LineGeom g;
-    return line_geometry(p, es, g) && (int64_t)p.N * p.OH < INT32_MAX &&
+    if (!line_geometry(p, es, g)) return false;
+    // weights, bias and tap tables in shared memory
+    if (line_smem(p, g) > 200 * 1024) return false;
+    return (int64_t)p.N * p.OH < INT32_MAX &&
            (g.CV + g.CVb - 1) / g.CVb <= 65535;   // channel chunks along grid y
 }
 
@@ -164,23 +311,36 @@ cudaError_t line_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *lau
     LineGeom g;
     if (!line_geometry(p, dtype_size(p.dtype), g)) return cudaErrorNotSupported;
     const int chunks = (g.CV + g.CVb - 1) / g.CVb;
-    int64_t bx = (g.items + g.PB - 1) / g.PB;
-    const int64_t cap = (int64_t)152 * 8 * 4 / chunks + 1;   // about 8 blocks per SM, 4 passes
-    if (bx > cap) bx = cap;
-    if (bx > INT32_MAX) bx = INT32_MAX;
+    const size_t smem = line_smem(p, g);
     return GCONV_DISPATCH_DTYPE(p.dtype, T, [&] {
-        constexpr int VEC = line_vec<T>();
-        const size_t smem = (size_t)(p.KH * p.KW + 1) * g.CVb * VEC * sizeof(float);
         auto go = [&](auto kernel) -> cudaError_t {
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);
             if (e != cudaSuccess) return e;
+            // Persistent blocks: as many as fit on the GPU at once, so the
+            // weight staging happens once per block; strips are grid-strided.
+            int per_sm = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel,
+                                                              g.CVb * g.PB, smem);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) per_sm = 1;
+            int64_t bx = (int64_t)152 * per_sm / chunks;
+            if (bx < 1) bx = 1;
+            const int64_t need = (g.items + g.PB - 1) / g.PB;
+            if (bx > need) bx = need;
+            if (bx > INT32_MAX) bx = INT32_MAX;
             e = launch_pdl(kernel, dim3((unsigned)bx, (unsigned)chunks), dim3(g.CVb * g.PB), smem,
                            s, static_cast<const T *>(q.x), static_cast<const T *>(q.w),
                            static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
             return e != cudaSuccess ? e : cudaGetLastError();
         };
-        return p.transposed ? go(line_kernel<T, true>) : go(line_kernel<T, false>);
+        const bool unit = !p.transposed && p.sw == 1 && p.dw == 1;
+        if (line_kwm(p.KW) == 4) {
+            if (p.transposed) return go(line_kernel<T, true, 4, false>);
+            return unit ? go(line_kernel<T, false, 4, true>) : go(line_kernel<T, false, 4, false>);
+        }
+        if (p.transposed) return go(line_kernel<T, true, 9, false>);
+        return unit ? go(line_kernel<T, false, 9, true>) : go(line_kernel<T, false, 9, false>);
     });
 }
 

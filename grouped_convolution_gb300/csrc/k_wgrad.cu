@@ -8,17 +8,19 @@
 // Two launches.  The first splits the output pixels (n, oh, ow) into slices
 // and writes one fp32 partial sum per (slice, co, tap) -- bias as one more
 // tap -- into the caller's workspace [slice][C_out][Cin_g*KH*KW + 1]; the
-// second adds each entry's slices in fp64 in slice order and rounds once
-// into dw (dense [C_out, Cin_g, KH, KW]) and db.  No atomics: the result is
-// the same on every run.
+// second adds each entry's slices in fp64 in a fixed order (eight
+// interleaved runs of slices, then the eight run sums) and rounds once into
+// dw (dense [C_out, Cin_g, KH, KW]) and db.  No atomics: the result is the
+// same on every run.
 //
 // Partial pass, two forms:
 //  - channels-last depthwise (one input and one output channel per group):
 //    a block owns a chunk of channel vectors and a slice of pixels; lane
 //    (cv, pixel lane) keeps CH channels x every tap in fp32 registers, walks
-//    its pixels (one gy vector load, one x vector load per tap in the input,
-//    packed FMAs), and the block adds its pixel lanes in shared memory, one
-//    tap at a time in a fixed order;
+//    its pixels (for each: the gy vector and the x vector of every tap in the
+//    input are loaded first, so they are in flight together, then packed
+//    FMAs), and the block adds its pixel lanes in shared memory, one tap at a
+//    time in a fixed order;
 //  - any other layout or group shape: a block owns (slice, co), every thread
 //    sums a tap over its pixels through the strides, and a fixed-order block
 //    reduction (shuffles, then shared memory) gives the slice's value.
@@ -34,10 +36,8 @@ constexpr int kWgThreads = 256;
 constexpr int kWgBlocksTarget = 152 * 4;
 
 // Channels per lane for the channels-last form: all taps of CH channels in
-// registers (at most about 100 fp32 accumulators).
-template <typename T, int TMAX> constexpr int wg_ch() {
-    return TMAX <= 9 ? 16 / (int)sizeof(T) : (TMAX <= 25 ? 4 : 2);
-}
+// fp32 registers, plus one load slot per tap.
+template <typename T, int TMAX> constexpr int wg_ch() { return TMAX <= 9 ? 4 : 2; }
 
 struct WgPlan {
     bool cl;          // channels-last depthwise form
@@ -48,7 +48,25 @@ struct WgPlan {
     int slices;
     int64_t P;        // output pixels N * OH * OW
     int T1;           // Cin_g * KH * KW + 1
+    FastDiv fd_ow, fd_oh;   // pixel index -> (n, oh, ow) when P < 2^32
 };
+
+// Output pixel q -> (n, oh, ow): multiply-high divisions when q fits in 32
+// bits (always, short of 2^32 pixels), 64-bit divisions otherwise.
+__device__ __forceinline__ void pixel_of(int64_t q, const Params &p, const WgPlan &pl, int &n,
+                                         int &oh, int &ow) {
+    if (pl.P <= (int64_t)0xFFFFFFFFu) {
+        uint32_t r, owu, nu, ohu;
+        pl.fd_ow.divmod((uint32_t)q, r, owu);
+        pl.fd_oh.divmod(r, nu, ohu);
+        n = (int)nu; oh = (int)ohu; ow = (int)owu;
+    } else {
+        ow = (int)(q % p.OW);
+        const int64_t r = q / p.OW;
+        oh = (int)(r % p.OH);
+        n = (int)(r / p.OH);
+    }
+}
 
 int cl_tmax(const Params &p) {
     const int taps = p.KH * p.KW;
@@ -56,8 +74,8 @@ int cl_tmax(const Params &p) {
 }
 
 int cl_ch(const Params &p, int tmax) {
-    const int es = dtype_size(p.dtype);
-    return tmax <= 9 ? 16 / es : (tmax <= 25 ? 4 : 2);
+    (void)p;
+    return tmax <= 9 ? 4 : 2;
 }
 
 // The shape half of the channels-last test (the pointer half is in
@@ -85,13 +103,16 @@ WgPlan plan_for(const Params &p, bool cl) {
     w.P = (int64_t)p.N * p.OH * p.OW;
     w.T1 = p.Cin_g * p.KH * p.KW + 1;
     w.cl = cl;
+    w.fd_ow = FastDiv((uint32_t)(p.OW > 0 ? p.OW : 1));
+    w.fd_oh = FastDiv((uint32_t)(p.OH > 0 ? p.OH : 1));
     if (cl) {
         w.tmax = cl_tmax(p);
         w.ch = cl_ch(p, w.tmax);
+        // Chunks of at most 32 channel vectors, balanced (36 vectors: 2 x 18).
         const int cv = p.C_out / w.ch;
-        w.CVb = cv < 32 ? cv : 32;
+        w.chunks = (int)cdiv(cv, 32);
+        w.CVb = (int)cdiv(cv, w.chunks);
         w.PL = kWgThreads / w.CVb;
-        w.chunks = (int)cdiv(cv, w.CVb);
         int64_t s = cdiv(kWgBlocksTarget, w.chunks);
         const int64_t most = cdiv(w.P, (int64_t)w.PL * 4);   // at least ~4 pixels per lane
         if (s > most) s = most;
@@ -143,33 +164,57 @@ wgrad_cl_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__rest
         for (int k = 0; k < PR; ++k) acc[tp][k] = make_float2(0.f, 0.f);
 
     if (active) {
-        for (int64_t q = p0 + lp; q < p1; q += pl.PL) {
-            const int ow = (int)(q % p.OW);
-            const int64_t r = q / p.OW;
-            const int oh = (int)(r % p.OH);
-            const int n = (int)(r / p.OH);
-            V gv;
-            IO::load(gv, gy + (int64_t)n * p.ys[0] + (int64_t)oh * p.ys[2] +
-                             (int64_t)ow * p.ys[3] + c0);
-            float2 g2[PR];
-            widen<T, CH>(gv, g2);
+        // U pixels per step (q, q + PL, ...; two for kernels of up to 9
+        // taps), their loads all issued before any arithmetic: gy and the x
+        // vector of every tap in the input.
+        constexpr int U = TMAX <= 9 ? 2 : 1;
+        for (int64_t q = p0 + lp; q < p1; q += U * pl.PL) {
+            V gv[U];
+            V xv[U][TMAX];
+            bool ok[U][TMAX];
+            bool have[U];
 #pragma unroll
-            for (int k = 0; k < PR; ++k) {
-                accb[k].x += g2[k].x;
-                accb[k].y += g2[k].y;
+            for (int u = 0; u < U; ++u) {
+                const int64_t qu = q + u * pl.PL;
+                have[u] = qu < p1;
+                int n, oh, ow;
+                pixel_of(have[u] ? qu : p0, p, pl, n, oh, ow);
+                if (have[u])
+                    IO::load(gv[u], gy + (int64_t)n * p.ys[0] + (int64_t)oh * p.ys[2] +
+                                        (int64_t)ow * p.ys[3] + c0);
+                const T *xn = x + (int64_t)n * p.xs[0] + c0;
+                const int ih0 = oh * p.sh - p.pbh, iw0 = ow * p.sw - p.pbw;
+                int kh = 0, kw = 0;   // tap tp = kh*KW + kw, stepped without divisions
+#pragma unroll
+                for (int tp = 0; tp < TMAX; ++tp) {
+                    ok[u][tp] = false;
+                    if (have[u] && tp < taps) {
+                        const int ih = ih0 + kh * p.dh, iw = iw0 + kw * p.dw;
+                        ok[u][tp] = ih >= 0 && ih < p.H && iw >= 0 && iw < p.W;
+                        if (ok[u][tp])
+                            IO::load(xv[u][tp], xn + (int64_t)ih * p.xs[2] + (int64_t)iw * p.xs[3]);
+                    }
+                    if (++kw == p.KW) {
+                        kw = 0;
+                        ++kh;
+                    }
+                }
             }
-            const T *xn = x + (int64_t)n * p.xs[0] + c0;
 #pragma unroll
-            for (int tp = 0; tp < TMAX; ++tp) {
-                if (tp < taps) {
-                    const int kh = tp / p.KW, kw = tp - kh * p.KW;
-                    const int ih = tap_input<false>(oh, kh, p.sh, p.pbh, p.dh, p.H);
-                    const int iw = tap_input<false>(ow, kw, p.sw, p.pbw, p.dw, p.W);
-                    if (ih >= 0 && iw >= 0) {
-                        V xv;
-                        IO::load(xv, xn + (int64_t)ih * p.xs[2] + (int64_t)iw * p.xs[3]);
+            for (int u = 0; u < U; ++u) {
+                if (!have[u]) continue;
+                float2 g2[PR];
+                widen<T, CH>(gv[u], g2);
+#pragma unroll
+                for (int k = 0; k < PR; ++k) {
+                    accb[k].x += g2[k].x;
+                    accb[k].y += g2[k].y;
+                }
+#pragma unroll
+                for (int tp = 0; tp < TMAX; ++tp) {
+                    if (ok[u][tp]) {
                         float2 x2[PR];
-                        widen<T, CH>(xv, x2);
+                        widen<T, CH>(xv[u][tp], x2);
 #pragma unroll
                         for (int k = 0; k < PR; ++k) fma2_packed(acc[tp][k], g2[k], x2[k]);
                     }
@@ -227,10 +272,8 @@ wgrad_generic_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *_
             const T *xc = x + (int64_t)(g * p.Cin_g + ci) * p.xs[1];
             float s = 0.f;
             for (int64_t q = p0 + t; q < p1; q += blockDim.x) {
-                const int ow = (int)(q % p.OW);
-                const int64_t r = q / p.OW;
-                const int oh = (int)(r % p.OH);
-                const int n = (int)(r / p.OH);
+                int n, oh, ow;
+                pixel_of(q, p, pl, n, oh, ow);
                 const float gv = load_f32(gy + (int64_t)n * p.ys[0] + (int64_t)co * p.ys[1] +
                                           (int64_t)oh * p.ys[2] + (int64_t)ow * p.ys[3]);
                 if (is_bias) {
@@ -258,22 +301,49 @@ wgrad_generic_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *_
     }
 }
 
+// Second pass: entry e = (co, tap) of the [C_out][T1] table is the sum of
+// its slices.  A block owns 32 entries (lanes) and its 8 warps take slices
+// g, g+8, g+16, ... (four loads in flight at a time), each adding in fp64
+// in slice order; warp 0 then adds the 8 warp sums in warp order.  The
+// order is fixed, so the result is the same on every run.
+constexpr int kFinEntries = 32, kFinGroups = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kFinEntries * kFinGroups)
 wgrad_finish_kernel(const float *__restrict__ ws, T *__restrict__ dw, T *__restrict__ db,
                     int C_out, int T1, int slices) {
     pdl_launch_dependents();
     pdl_wait();
+    __shared__ double part[kFinGroups][kFinEntries];
+    const int lane = threadIdx.x % kFinEntries, grp = threadIdx.x / kFinEntries;
     const int64_t total = (int64_t)C_out * T1;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        double s = 0.0;
-        for (int sl = 0; sl < slices; ++sl) s += (double)ws[(int64_t)sl * total + e];
+    const int64_t e = (int64_t)blockIdx.x * kFinEntries + lane;
+    double s = 0.0;
+    if (e < total) {
+        int sl = grp;
+        for (; sl + 3 * kFinGroups < slices; sl += 4 * kFinGroups) {
+            const float a = ws[(int64_t)sl * total + e];
+            const float b = ws[(int64_t)(sl + kFinGroups) * total + e];
+            const float c = ws[(int64_t)(sl + 2 * kFinGroups) * total + e];
+            const float d = ws[(int64_t)(sl + 3 * kFinGroups) * total + e];
+            s += (double)a;
+            s += (double)b;
+            s += (double)c;
+            s += (double)d;
+        }
+        for (; sl < slices; sl += kFinGroups) s += (double)ws[(int64_t)sl * total + e];
+    }
+    part[grp][lane] = s;
+    __syncthreads();
+    if (grp == 0 && e < total) {
+        double tot = 0.0;
+#pragma unroll
+        for (int g = 0; g < kFinGroups; ++g) tot += part[g][lane];
         const int co = (int)(e / T1), tap = (int)(e - (int64_t)co * T1);
         if (tap < T1 - 1)
-            dw[(int64_t)co * (T1 - 1) + tap] = from_f32<T>((float)s);
+            dw[(int64_t)co * (T1 - 1) + tap] = from_f32<T>((float)tot);
         else if (db)
-            db[co] = from_f32<T>((float)s);
+            db[co] = from_f32<T>((float)tot);
     }
 }
 
@@ -321,11 +391,11 @@ cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *d
         }
         if (e != cudaSuccess) return e;
         const int64_t total = (int64_t)p.C_out * pl.T1;
-        int64_t blocks = (total + 255) / 256;
-        if (blocks > 152 * 8) blocks = 152 * 8;
-        e = launch_pdl(wgrad_finish_kernel<T>, dim3((unsigned)blocks), dim3(256), 0, s,
-                       (const float *)ws, static_cast<T *>(dw), static_cast<T *>(db), p.C_out,
-                       pl.T1, pl.slices);
+        const int64_t blocks = (total + kFinEntries - 1) / kFinEntries;
+        if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+        e = launch_pdl(wgrad_finish_kernel<T>, dim3((unsigned)blocks),
+                       dim3(kFinEntries * kFinGroups), 0, s, (const float *)ws,
+                       static_cast<T *>(dw), static_cast<T *>(db), p.C_out, pl.T1, pl.slices);
         return e != cudaSuccess ? e : cudaGetLastError();
     });
 }
