@@ -25,7 +25,9 @@
 // consecutive q all read tap k at input q + c(ph, k) (c from a per-block
 // table of (phase, tap) offsets, none when that phase skips the tap), so a
 // strip needs no division and reads consecutive inputs; the output row's
-// taps come from a second table the same way.
+// taps come from a second table the same way.  With dilation 1 the taps of
+// a phase sit s apart and their offsets one apart, so the strip's inputs
+// form one register window too.
 // Forward calls with stride 1 and dilation 1 keep a register sliding window
 // instead: the S + KW - 1 input vectors of a strip's row are loaded and
 // widened once, and every tap reads its S vectors from the window.
@@ -53,6 +55,7 @@ struct LineGeom {
     int NSW;     // strips per output row (per column phase when transposed)
     int64_t items;   // N * OH * NSW (* stride_w when transposed), < 2^31
     int tab_w, tab_h;   // transposed: offsets of the column / row tap tables (ints)
+    int tab_p;          // transposed, dilation 1: per column phase (last tap, its offset)
     FastDiv fd_nsw, fd_sw, fd_oh, fd_sh;   // item decomposition without divisions
 };
 
@@ -80,6 +83,7 @@ bool line_geometry(const Params &p, int es, LineGeom &g) {
     const int cb = g.CVb * vec;
     g.tab_w = (p.KH * p.KW + 1) * cb;            // after the fp32 weights (same 4-byte units)
     g.tab_h = g.tab_w + (p.transposed ? p.sw * p.KW : 0);
+    g.tab_p = g.tab_h + (p.transposed ? p.sh * p.KH : 0);
     g.fd_nsw = FastDiv((uint32_t)g.NSW);
     g.fd_sw = FastDiv((uint32_t)p.sw);
     g.fd_oh = FastDiv((uint32_t)p.OH);
@@ -88,7 +92,7 @@ bool line_geometry(const Params &p, int es, LineGeom &g) {
 }
 
 size_t line_smem(const Params &p, const LineGeom &g) {
-    return (size_t)(g.tab_h + (p.transposed ? p.sh * p.KH : 0)) * 4;
+    return (size_t)(g.tab_p + (p.transposed ? 2 * p.sw : 0)) * 4;
 }
 
 // Transposed tap table entry: for phase r (0 <= r < s) and tap k, the
@@ -100,6 +104,8 @@ __device__ __forceinline__ int tr_offset(int r, int k, int s, int pb, int d) {
     return (num % s == 0) ? num / s : kNoTap;
 }
 
+// UNIT: the register-window form (forward: stride 1 and dilation 1;
+// transposed: dilation 1).
 template <typename T, bool TR, int KWM, bool UNIT>
 __global__ void __launch_bounds__(kLineThreads)
 line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
@@ -118,6 +124,7 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
     extern __shared__ __align__(16) float line_w[];
     int *tab_w = reinterpret_cast<int *>(line_w) + g.tab_w;
     int *tab_h = reinterpret_cast<int *>(line_w) + g.tab_h;
+    int *tab_p = reinterpret_cast<int *>(line_w) + g.tab_p;
 
     const int taps = p.KH * p.KW;
     const int cb = g.CVb * VEC;                  // channels per block
@@ -144,6 +151,22 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
             tab_w[e] = tr_offset(e / p.KW, e % p.KW, p.sw, p.pbw, p.dw);
         for (int e = t; e < p.sh * p.KH; e += blockDim.x)
             tab_h[e] = tr_offset(e / p.KH, e % p.KH, p.sh, p.pbh, p.dh);
+        // With dilation 1 the taps a column phase reads are kw_last,
+        // kw_last - s, ... and their offsets c_min, c_min + 1, ...: the
+        // strip's inputs form one window (phase with no tap: kw_last = -1).
+        for (int ph = t; ph < p.sw; ph += blockDim.x) {
+            int last = -1, cmin = 0;
+            for (int kw = p.KW - 1; kw >= 0; --kw) {
+                const int c = tr_offset(ph, kw, p.sw, p.pbw, 1);
+                if (c != kNoTap) {
+                    last = kw;
+                    cmin = c;
+                    break;
+                }
+            }
+            tab_p[2 * ph] = last;
+            tab_p[2 * ph + 1] = cmin;
+        }
     }
     __syncthreads();
 
@@ -203,7 +226,46 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
             }
             if (ih < 0) continue;
             const T *xr = xn + (int64_t)ih * p.xs[2];
-            if constexpr (UNIT) {
+            if constexpr (TR && UNIT) {
+                {
+                    // The phase's j-th tap from the last (kw = kw_last - j*s)
+                    // reads input q + c_min + j: a window of S + nv - 1
+                    // vectors, tap j and pixel i at slot j + i.
+                    constexpr int NW = S + KWM - 1;
+                    const int last = tab_p[2 * ph], cmin = tab_p[2 * ph + 1];
+                    const int nv = last < 0 ? 0 : last / p.sw + 1;
+                    float2 win[NW][P];
+                    const int iw0 = q0 + cmin;
+#pragma unroll
+                    for (int m = 0; m < NW; ++m) {
+                        const int iw = iw0 + m;
+                        if (m < S + nv - 1 && iw >= 0 && iw < p.W) {
+                            V v;
+                            IO::load(v, xr + (int64_t)iw * p.xs[3]);
+                            widen<T, VEC>(v, win[m]);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < P; ++k) win[m][k] = make_float2(0.f, 0.f);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < KWM; ++j) {
+                        if (j >= nv) break;
+                        const int kw = last - j * p.sw;
+                        float2 wk[P];
+                        const float2 *src = wv + ((kh * p.KW + kw) * cb) / 2;
+#pragma unroll
+                        for (int k = 0; k < P; ++k) wk[k] = src[k];
+#pragma unroll
+                        for (int i = 0; i < S; ++i)
+#pragma unroll
+                            for (int k = 0; k < P; ++k)
+                                fma2_packed(acc[i][k], wk[k], win[j + i][k]);
+                    }
+                    continue;
+                }
+            }
+            if constexpr (!TR && UNIT) {
                 // Stride 1, dilation 1: the strip's S + KW - 1 input vectors
                 // form one window; each is loaded and widened once and
                 // slides under the taps.
@@ -334,13 +396,17 @@ cudaError_t line_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *lau
                            static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
             return e != cudaSuccess ? e : cudaGetLastError();
         };
-        const bool unit = !p.transposed && p.sw == 1 && p.dw == 1;
+        // The window forms: forward with stride 1 and dilation 1, transposed
+        // with dilation 1.
+        const bool win = p.transposed ? p.dw == 1 : (p.sw == 1 && p.dw == 1);
         if (line_kwm(p.KW) == 4) {
-            if (p.transposed) return go(line_kernel<T, true, 4, false>);
-            return unit ? go(line_kernel<T, false, 4, true>) : go(line_kernel<T, false, 4, false>);
+            if (p.transposed)
+                return win ? go(line_kernel<T, true, 4, true>) : go(line_kernel<T, true, 4, false>);
+            return win ? go(line_kernel<T, false, 4, true>) : go(line_kernel<T, false, 4, false>);
         }
-        if (p.transposed) return go(line_kernel<T, true, 9, false>);
-        return unit ? go(line_kernel<T, false, 9, true>) : go(line_kernel<T, false, 9, false>);
+        if (p.transposed)
+            return win ? go(line_kernel<T, true, 9, true>) : go(line_kernel<T, true, 9, false>);
+        return win ? go(line_kernel<T, false, 9, true>) : go(line_kernel<T, false, 9, false>);
     });
 }
 
