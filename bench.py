@@ -201,6 +201,7 @@ KERNEL_SOURCES = {
     "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh", "launch.cuh"],
     "grp_reduce": ["k_reduce.cu", "device_common.cuh", "launch.cuh"],
     "grp_tc": ["k_tc.cu", "device_common.cuh", "tma.cuh", "launch.cuh"],
+    "dw_line": ["k_line.cu", "stencil_math.cuh", "device_common.cuh", "launch.cuh"],
 }
 
 
