@@ -391,7 +391,10 @@ def time_e2e(cases, steps, world, lanes=3):
     streams = [torch.cuda.Stream() for _ in range(lanes)]
     dev_x = [cases[0].xs[0]] + [cases[0].xs[0].clone() for _ in range(lanes - 1)]
     dev_y = [[gc.empty_output(c.desc, dev_x[0]) for c in cases] for _ in range(lanes)]
-    outs = [[torch.empty(c.ys[0].shape, dtype=c.ys[0].dtype).pin_memory() for c in cases]
+    # Pinned host outputs with the device outputs' own strides (channels-last
+    # stays channels-last), so each read-back is one plain copy.
+    outs = [[torch.empty_strided(c.ys[0].shape, c.ys[0].stride(), dtype=c.ys[0].dtype,
+                                 pin_memory=True) for c in cases]
             for _ in range(lanes)]
     h2d = host_x.numel() * host_x.element_size()
     d2h = sum(o.numel() * o.element_size() for o in outs[0])
