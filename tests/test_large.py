@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     # name, N, C_in, H, W, Cin_g, Cout_g, K, stride, pad, dtype, schedules
-    ("dw3x3_bf16_cl", 16, 1024, 400, 400, 1, 1, 3, 1, 1, torch.bfloat16, ["dw_row8", "dw_flat"]),
+    ("dw3x3_bf16_cl", 16, 1024, 400, 400, 1, 1, 3, 1, 1, torch.bfloat16,
+     ["dw_row8", "dw_flat", "dw_line"]),
     ("dw3x3_f16_nchw", 12, 1024, 420, 420, 1, 1, 3, 1, 1, torch.float16, ["dw_mult"]),
     ("grp4x8_9x9_bf16_cl", 64, 256, 384, 384, 4, 8, 9, 2, 4, torch.bfloat16, ["grp_tc"]),
 ]
