@@ -28,9 +28,11 @@
 // taps come from a second table the same way.  With dilation 1 the taps of
 // a phase sit s apart and their offsets one apart, so the strip's inputs
 // form one register window too.
-// Forward calls with stride 1 and dilation 1 keep a register sliding window
-// instead: the S + KW - 1 input vectors of a strip's row are loaded and
-// widened once, and every tap reads its S vectors from the window.
+// Forward calls with stride 1 keep a register sliding window instead: the
+// S + KW - 1 input vectors of a strip's row are loaded and widened once, and
+// every tap reads its S vectors from the window; with dilation d a strip
+// holds outputs d apart (one column phase), so its taps still slide over
+// consecutive window slots.
 #include "device_common.cuh"
 #include "gconv_internal.h"
 #include "launch.cuh"
@@ -52,11 +54,13 @@ struct LineGeom {
     int CV;      // channel vectors in the tensor
     int CVb;     // channel vectors per block (lanes along channels)
     int PB;      // strips per block pass (lanes along pixels)
-    int NSW;     // strips per output row (per column phase when transposed)
-    int64_t items;   // N * OH * NSW (* stride_w when transposed), < 2^31
+    int PH;      // column phases: stride_w (transposed), dilation_w (forward at
+                 // stride 1: the window form walks one phase), else 1
+    int NSW;     // strips per output row and phase
+    int64_t items;   // N * OH * PH * NSW, < 2^31
     int tab_w, tab_h;   // transposed: offsets of the column / row tap tables (ints)
     int tab_p;          // transposed, dilation 1: per column phase (last tap, its offset)
-    FastDiv fd_nsw, fd_sw, fd_oh, fd_sh;   // item decomposition without divisions
+    FastDiv fd_nsw, fd_ph, fd_oh, fd_sh;   // item decomposition without divisions
 };
 
 // Tap tables of a transposed call (entries per phase x tap) must fit here.
@@ -70,22 +74,20 @@ bool line_geometry(const Params &p, int es, LineGeom &g) {
     const int chunks = (g.CV + 31) / 32;         // balanced chunks of <= 32 vectors
     g.CVb = (g.CV + chunks - 1) / chunks;
     g.PB = kLineThreads / g.CVb;
-    if (p.transposed) {
-        // Strips of one column phase ph: outputs q*sw + ph for S consecutive q.
-        const int Q = (p.OW + p.sw - 1) / p.sw;
-        g.NSW = (Q + S - 1) / S;
-        g.items = (int64_t)p.N * p.OH * p.sw * g.NSW;
-        if ((int64_t)p.sw * p.KW > kLineTabMax || (int64_t)p.sh * p.KH > kLineTabMax) return false;
-    } else {
-        g.NSW = (p.OW + S - 1) / S;
-        g.items = (int64_t)p.N * p.OH * g.NSW;
-    }
+    // Strips of one column phase ph: outputs q*PH + ph for S consecutive q.
+    g.PH = p.transposed ? p.sw : (p.sw == 1 ? p.dw : 1);
+    const int Q = (p.OW + g.PH - 1) / g.PH;
+    g.NSW = (Q + S - 1) / S;
+    g.items = (int64_t)p.N * p.OH * g.PH * g.NSW;
+    if (p.transposed &&
+        ((int64_t)p.sw * p.KW > kLineTabMax || (int64_t)p.sh * p.KH > kLineTabMax))
+        return false;
     const int cb = g.CVb * vec;
     g.tab_w = (p.KH * p.KW + 1) * cb;            // after the fp32 weights (same 4-byte units)
     g.tab_h = g.tab_w + (p.transposed ? p.sw * p.KW : 0);
     g.tab_p = g.tab_h + (p.transposed ? p.sh * p.KH : 0);
     g.fd_nsw = FastDiv((uint32_t)g.NSW);
-    g.fd_sw = FastDiv((uint32_t)p.sw);
+    g.fd_ph = FastDiv((uint32_t)g.PH);
     g.fd_oh = FastDiv((uint32_t)p.OH);
     g.fd_sh = FastDiv((uint32_t)p.sh);
     return g.CV >= 1 && g.items <= INT32_MAX;
@@ -104,8 +106,7 @@ __device__ __forceinline__ int tr_offset(int r, int k, int s, int pb, int d) {
     return (num % s == 0) ? num / s : kNoTap;
 }
 
-// UNIT: the register-window form (forward: stride 1 and dilation 1;
-// transposed: dilation 1).
+// UNIT: the register-window form (forward: stride 1; transposed: dilation 1).
 template <typename T, bool TR, int KWM, bool UNIT>
 __global__ void __launch_bounds__(kLineThreads)
 line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
@@ -188,9 +189,9 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
         g.fd_nsw.divmod(item, r, sxu);
         const int sx = (int)sxu;
         int ph = 0;
-        if constexpr (TR) {
+        if constexpr (TR || UNIT) {
             uint32_t r2, phu;
-            g.fd_sw.divmod(r, r2, phu);
+            g.fd_ph.divmod(r, r2, phu);
             ph = (int)phu;
             r = r2;
         }
@@ -198,9 +199,9 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
         g.fd_oh.divmod(r, nu, ohu);
         const int oh = (int)ohu;
         const int n = (int)nu;
-        const int ostep = TR ? p.sw : 1;
-        const int q0 = sx * S;                   // transposed: first q of the strip
-        const int ow0 = TR ? q0 * p.sw + ph : q0;
+        const int ostep = g.PH;
+        const int q0 = sx * S;                   // first q of the strip
+        const int ow0 = q0 * g.PH + ph;
         float2 acc[S][P];
 #pragma unroll
         for (int i = 0; i < S; ++i)
@@ -266,15 +267,16 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
                 }
             }
             if constexpr (!TR && UNIT) {
-                // Stride 1, dilation 1: the strip's S + KW - 1 input vectors
-                // form one window; each is loaded and widened once and
-                // slides under the taps.
+                // Stride 1: the strip's outputs (q0 + i)*d + ph at tap kw read
+                // input (q0 + i + kw)*d + ph - pb, so its S + KW - 1 input
+                // vectors form one window; each is loaded and widened once
+                // and slides under the taps.
                 constexpr int NW = S + KWM - 1;
                 float2 win[NW][P];
                 const int iw0 = ow0 - p.pbw;
 #pragma unroll
                 for (int j = 0; j < NW; ++j) {
-                    const int iw = iw0 + j;
+                    const int iw = iw0 + j * p.dw;
                     if (j < S + p.KW - 1 && iw >= 0 && iw < p.W) {
                         V v;
                         IO::load(v, xr + (int64_t)iw * p.xs[3]);
@@ -396,9 +398,9 @@ cudaError_t line_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *lau
                            static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
             return e != cudaSuccess ? e : cudaGetLastError();
         };
-        // The window forms: forward with stride 1 and dilation 1, transposed
-        // with dilation 1.
-        const bool win = p.transposed ? p.dw == 1 : (p.sw == 1 && p.dw == 1);
+        // The window forms: forward with stride 1 (one column phase per
+        // strip when dilated), transposed with dilation 1.
+        const bool win = p.transposed ? p.dw == 1 : p.sw == 1;
         if (line_kwm(p.KW) == 4) {
             if (p.transposed)
                 return win ? go(line_kernel<T, true, 4, true>) : go(line_kernel<T, true, 4, false>);
