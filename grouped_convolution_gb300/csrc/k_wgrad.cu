@@ -13,7 +13,7 @@
 // dw (dense [C_out, Cin_g, KH, KW]) and db.  No atomics: the result is the
 // same on every run.
 //
-// Partial pass, two forms:
+// Partial pass, three forms:
 //  - channels-last depthwise (one input and one output channel per group):
 //    a block owns a chunk of channel vectors and a slice of pixels; lane
 //    (cv, pixel lane) keeps CH channels x every tap in fp32 registers, walks
@@ -21,6 +21,9 @@
 //    input are loaded first, so they are in flight together, then packed
 //    FMAs), and the block adds its pixel lanes in shared memory, one tap at a
 //    time in a fixed order;
+//  - the same at column stride 1 with kernels of at most 3 x 3 (or 1 x 9):
+//    strips of 4 outputs that share one register window of inputs per
+//    kernel row (wgrad_strip_kernel);
 //  - any other layout or group shape: a block owns (slice, co), every thread
 //    sums a tap over its pixels through the strides, and a fixed-order block
 //    reduction (shuffles, then shared memory) gives the slice's value.
@@ -49,7 +52,14 @@ struct WgPlan {
     int64_t P;        // output pixels N * OH * OW
     int T1;           // Cin_g * KH * KW + 1
     FastDiv fd_ow, fd_oh;   // pixel index -> (n, oh, ow) when P < 2^32
+    // strip form: items (n, oh, column phase, strip of kWgS outputs)
+    int strip;        // 0: per-pixel form; 33 or 19: strip form for KH<=3,KW<=3 / KH=1,KW<=9
+    int PH, NSW;
+    int64_t items;
+    FastDiv fd_nsw, fd_ph;
 };
+
+constexpr int kWgS = 4;   // output pixels per strip (strip form)
 
 // Output pixel q -> (n, oh, ow): multiply-high divisions when q fits in 32
 // bits (always, short of 2^32 pixels), 64-bit divisions otherwise.
@@ -98,14 +108,41 @@ bool wg_cl_pointers(const Params &p, const void *x, const void *gy, int ch) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-WgPlan plan_for(const Params &p, bool cl) {
+// The strip form takes channels-last depthwise calls at column stride 1 with
+// kernels of at most 3 x 3, or height 1 and width at most 9.
+int strip_kind(const Params &p) {
+    if (!cl_shape(p) || p.sw != 1) return 0;
+    if (p.KH <= 3 && p.KW <= 3) return 33;
+    if (p.KH == 1 && p.KW <= 9) return 19;
+    return 0;
+}
+
+WgPlan plan_for(const Params &p, bool cl, int strip = 0) {
     WgPlan w{};
     w.P = (int64_t)p.N * p.OH * p.OW;
     w.T1 = p.Cin_g * p.KH * p.KW + 1;
     w.cl = cl;
     w.fd_ow = FastDiv((uint32_t)(p.OW > 0 ? p.OW : 1));
     w.fd_oh = FastDiv((uint32_t)(p.OH > 0 ? p.OH : 1));
-    if (cl) {
+    if (strip) {
+        // 4 channels a lane; strips of kWgS outputs of one column phase.
+        w.strip = strip;
+        w.ch = 4;
+        const int cv = p.C_out / w.ch;
+        w.chunks = (int)cdiv(cv, 32);
+        w.CVb = (int)cdiv(cv, w.chunks);
+        w.PL = kWgThreads / w.CVb;
+        w.PH = p.dw;
+        const int Q = (p.OW + w.PH - 1) / w.PH;
+        w.NSW = (Q + kWgS - 1) / kWgS;
+        w.items = (int64_t)p.N * p.OH * w.PH * w.NSW;
+        w.fd_nsw = FastDiv((uint32_t)w.NSW);
+        w.fd_ph = FastDiv((uint32_t)w.PH);
+        int64_t s = cdiv(kWgBlocksTarget, w.chunks);
+        const int64_t most = cdiv(w.items, (int64_t)w.PL * 2);   // at least ~2 strips per lane
+        if (s > most) s = most;
+        w.slices = (int)(s < 1 ? 1 : s);
+    } else if (cl) {
         w.tmax = cl_tmax(p);
         w.ch = cl_ch(p, w.tmax);
         // Chunks of at most 32 channel vectors, balanced (36 vectors: 2 x 18).
@@ -301,6 +338,135 @@ wgrad_generic_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *_
     }
 }
 
+// Strip form of the partial pass: lane (cv, strip lane) walks items
+// (n, oh, column phase ph, strip of kWgS outputs ow = (q0 + i)*d + ph).  Per
+// item it loads the strip's gy vectors once, and for each kernel row the
+// strip's window of kWgS + KW - 1 input vectors (output i at tap kw reads
+// slot i + kw), so a pixel costs 1 + KH*(kWgS + KW - 1)/kWgS vector loads
+// instead of 1 + KH*KW, all of a row in flight together.
+template <typename T, int KHM, int KWM>
+__global__ void __launch_bounds__(kWgThreads)
+wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__restrict__ ws,
+                   Params p, WgPlan pl) {
+    pdl_launch_dependents();
+    pdl_wait();
+    constexpr int CH = 4;
+    constexpr int PR = CH / 2;
+    constexpr int S = kWgS;
+    constexpr int NW = S + KWM - 1;
+    using V = Vec<T, CH>;
+    using IO = VecIO<CH * (int)sizeof(T)>;
+    __shared__ float red[kWgThreads * CH];        // [pixel lane][block channel]
+
+    const int t = threadIdx.x;
+    const int cvl = t % pl.CVb, lp = t / pl.CVb;
+    const int cv = blockIdx.y * pl.CVb + cvl;
+    const bool active = lp < pl.PL && cv * CH < p.C_out;
+    const int c0 = cv * CH;
+    int64_t i0, i1;
+    slice_range(pl.items, pl.slices, blockIdx.x, i0, i1);
+
+    float2 acc[KHM][KWM][PR];
+    float2 accb[PR];
+#pragma unroll
+    for (int k = 0; k < PR; ++k) accb[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int a = 0; a < KHM; ++a)
+#pragma unroll
+        for (int c = 0; c < KWM; ++c)
+#pragma unroll
+            for (int k = 0; k < PR; ++k) acc[a][c][k] = make_float2(0.f, 0.f);
+
+    if (active) {
+        for (int64_t item = i0 + lp; item < i1; item += pl.PL) {
+            uint32_t r, sxu, r2, phu, nu, ohu;
+            pl.fd_nsw.divmod((uint32_t)item, r, sxu);
+            pl.fd_ph.divmod(r, r2, phu);
+            pl.fd_oh.divmod(r2, nu, ohu);
+            const int oh = (int)ohu, n = (int)nu;
+            const int ow0 = (int)sxu * S * pl.PH + (int)phu;
+            float2 g[S][PR];
+#pragma unroll
+            for (int i = 0; i < S; ++i) {
+                const int ow = ow0 + i * pl.PH;
+                if (ow < p.OW) {
+                    V v;
+                    IO::load(v, gy + (int64_t)n * p.ys[0] + (int64_t)oh * p.ys[2] +
+                                    (int64_t)ow * p.ys[3] + c0);
+                    widen<T, CH>(v, g[i]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < PR; ++k) g[i][k] = make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int k = 0; k < PR; ++k) {
+                    accb[k].x += g[i][k].x;
+                    accb[k].y += g[i][k].y;
+                }
+            }
+            const T *xn = x + (int64_t)n * p.xs[0] + c0;
+            const int iw0 = ow0 - p.pbw;
+#pragma unroll
+            for (int kh = 0; kh < KHM; ++kh) {
+                if (kh >= p.KH) break;
+                const int ih = oh * p.sh - p.pbh + kh * p.dh;
+                if (ih < 0 || ih >= p.H) continue;
+                const T *xr = xn + (int64_t)ih * p.xs[2];
+                float2 win[NW][PR];
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    const int iw = iw0 + j * p.dw;
+                    if (j < S + p.KW - 1 && iw >= 0 && iw < p.W) {
+                        V v;
+                        IO::load(v, xr + (int64_t)iw * p.xs[3]);
+                        widen<T, CH>(v, win[j]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < PR; ++k) win[j][k] = make_float2(0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int kw = 0; kw < KWM; ++kw) {
+                    if (kw >= p.KW) break;
+#pragma unroll
+                    for (int i = 0; i < S; ++i)
+#pragma unroll
+                        for (int k = 0; k < PR; ++k)
+                            fma2_packed(acc[kh][kw][k], g[i][k], win[i + kw][k]);
+                }
+            }
+        }
+    }
+    // Add the pixel lanes, one tap (then the bias) at a time, lanes in order.
+    const int cb = pl.CVb * CH;
+    const int c_first = blockIdx.y * cb;
+#pragma unroll
+    for (int tp = 0; tp <= KHM * KWM; ++tp) {
+        const bool bias_slot = tp == KHM * KWM;
+        const int kh = bias_slot ? 0 : tp / KWM, kw = bias_slot ? 0 : tp % KWM;
+        if (!bias_slot && (kh >= p.KH || kw >= p.KW)) continue;   // the same for the block
+        const float2 *src = bias_slot ? accb : acc[kh][kw];
+        const int slot = bias_slot ? p.KH * p.KW : kh * p.KW + kw;
+        if (lp < pl.PL) {
+#pragma unroll
+            for (int k = 0; k < PR; ++k) {
+                red[lp * cb + cvl * CH + 2 * k] = src[k].x;
+                red[lp * cb + cvl * CH + 2 * k + 1] = src[k].y;
+            }
+        }
+        __syncthreads();
+        for (int e = t; e < cb; e += blockDim.x) {
+            const int c = c_first + e;
+            if (c < p.C_out) {
+                float sum = 0.f;
+                for (int l = 0; l < pl.PL; ++l) sum += red[l * cb + e];
+                ws[((int64_t)blockIdx.x * p.C_out + c) * pl.T1 + slot] = sum;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // Second pass: entry e = (co, tap) of the [C_out][T1] table is the sum of
 // its slices.  A block owns 32 entries (lanes) and its 8 warps take slices
 // g, g+8, g+16, ... (four loads in flight at a time), each adding in fp64
@@ -364,6 +530,11 @@ uint64_t wgrad_workspace_bytes(const Params &p) {
     if (cl_shape(p)) {
         const WgPlan c = plan_for(p, true);
         if (c.slices > slices) slices = c.slices;
+        const int sk = strip_kind(p);
+        if (sk && (int64_t)p.N * p.OH * p.OW < 0xFFFFFFFFll) {
+            const WgPlan st = plan_for(p, true, sk);
+            if (st.slices > slices) slices = st.slices;
+        }
     }
     uint64_t b = (uint64_t)slices * (uint64_t)(p.C_out > 0 ? p.C_out : 0) * (uint64_t)g.T1 * 4u;
     return b < 16 ? 16 : b;
@@ -374,13 +545,23 @@ cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *d
     *launches = 2;
     bool cl = cl_shape(p);
     if (cl) cl = wg_cl_pointers(p, x, gy, cl_ch(p, cl_tmax(p)));
-    const WgPlan pl = plan_for(p, cl);
+    // The strip form (4-channel loads, items counted in 32 bits).
+    int sk = cl ? strip_kind(p) : 0;
+    if (sk && !(wg_cl_pointers(p, x, gy, 4) && (int64_t)p.N * p.OH * p.OW < 0xFFFFFFFFll))
+        sk = 0;
+    const WgPlan pl = plan_for(p, cl, sk);
     float *ws = static_cast<float *>(workspace);
     return GCONV_DISPATCH_DTYPE(p.dtype, T, [&] {
         const T *xt = static_cast<const T *>(x);
         const T *gt = static_cast<const T *>(gy);
         cudaError_t e;
-        if (cl) {
+        if (sk == 33) {
+            e = launch_pdl(wgrad_strip_kernel<T, 3, 3>, dim3(pl.slices, pl.chunks),
+                           dim3(pl.CVb * pl.PL), 0, s, xt, gt, ws, p, pl);
+        } else if (sk == 19) {
+            e = launch_pdl(wgrad_strip_kernel<T, 1, 9>, dim3(pl.slices, pl.chunks),
+                           dim3(pl.CVb * pl.PL), 0, s, xt, gt, ws, p, pl);
+        } else if (cl) {
             if (pl.tmax == 9) e = launch_cl<T, 9>(p, xt, gt, ws, pl, s);
             else if (pl.tmax == 25) e = launch_cl<T, 25>(p, xt, gt, ws, pl, s);
             else e = launch_cl<T, 49>(p, xt, gt, ws, pl, s);

@@ -195,6 +195,9 @@ BWD = [
     ("m4_4x4", 2, 1, 4, 8, 11, 10, 4, 4, (1, 1), (1, 1), (2, 2), (1, 1)),
     ("g4x8_9x9_s2", 1, 4, 8, 4, 17, 18, 9, 9, (2, 2), (4, 4), (4, 4), (1, 1)),
     ("g2x3_3x3", 2, 2, 3, 5, 9, 9, 3, 3, (1, 1), (1, 1), (1, 1), (1, 1)),
+    ("dw1x7_s1", 2, 1, 1, 40, 5, 30, 1, 7, (1, 1), (0, 3), (0, 3), (1, 1)),
+    ("dw2x2_s1_ragged", 3, 1, 1, 24, 7, 13, 2, 2, (2, 1), (0, 1), (1, 0), (1, 1)),
+    ("dw1x3_d3", 1, 1, 1, 32, 4, 29, 1, 3, (1, 1), (0, 3), (0, 3), (1, 3)),
 ]
 
 
