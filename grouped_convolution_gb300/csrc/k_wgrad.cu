@@ -36,7 +36,7 @@ namespace gconv {
 namespace {
 
 constexpr int kWgThreads = 256;
-constexpr int kWgBlocksTarget = 152 * 4;
+constexpr int kWgBlocksTarget = 152 * 2;   // measured: 4 and 8 per SM are slower (more slices to add)
 
 // Channels per lane for the channels-last form: all taps of CH channels in
 // fp32 registers, plus one load slot per tap.
