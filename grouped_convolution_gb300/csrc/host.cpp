@@ -455,15 +455,26 @@ struct Plan {
     int32_t schedule;
 };
 
-// A stride-1 transposed convolution with one input channel per group is the
-// forward convolution of the same input with the kernel flipped in both
-// dims, output channel co = g*Cout_g + j reading weight w[g, j] (a stride
-// over co when Cout_g == 1 or the weight's first two strides nest), padding
-// d*(K-1) - crop before and d*(K-1) + output_padding - crop after (both must
-// be >= 0):  y[o] = sum_k w[k] x[o + crop - k*d] = sum_k' w[K-1-k'] x[o - pad + k'*d].
+// A stride-1 transposed convolution is the forward convolution of the same
+// input with the kernel flipped in both dims, padding d*(K-1) - crop before
+// and d*(K-1) + output_padding - crop after (both must be >= 0):
+//   y[o] = sum_k w[k] x[o + crop - k*d] = sum_k' w[K-1-k'] x[o - pad + k'*d].
+// Output channel co = g*Cout_g + j reads weight w[g*Cin_g + ci, j]; that is a
+// stride over (co, ci) when each group has one output channel (co stride
+// Cin_g * ws0, ci stride ws0) or one input channel and nesting weight strides
+// (co stride ws1).
 static bool flipped_forward(const gconv_desc &t, const Ptrs &p, gconv_desc *f, Ptrs *q) {
-    if (!t.transposed || t.stride[0] != 1 || t.stride[1] != 1 || t.Cin_g != 1) return false;
-    if (t.Cout_g != 1 && t.w_strides[0] != t.Cout_g * t.w_strides[1]) return false;
+    if (!t.transposed || t.stride[0] != 1 || t.stride[1] != 1) return false;
+    int64_t co_stride, ci_stride;
+    if (t.Cout_g == 1) {
+        co_stride = t.Cin_g * t.w_strides[0];
+        ci_stride = t.w_strides[0];
+    } else if (t.Cin_g == 1 && t.w_strides[0] == t.Cout_g * t.w_strides[1]) {
+        co_stride = t.w_strides[1];
+        ci_stride = t.w_strides[0];   // one input channel: unused
+    } else {
+        return false;
+    }
     const int64_t ext_h = (int64_t)t.dilation[0] * (t.KH - 1);
     const int64_t ext_w = (int64_t)t.dilation[1] * (t.KW - 1);
     const int64_t pbh = ext_h - t.pad_before[0], pbw = ext_w - t.pad_before[1];
@@ -473,12 +484,10 @@ static bool flipped_forward(const gconv_desc &t, const Ptrs &p, gconv_desc *f, P
     *f = t;
     f->transposed = 0;
     f->output_padding[0] = f->output_padding[1] = 0;
-    f->Cin_g = 1;
     f->pad_before[0] = (int32_t)pbh; f->pad_before[1] = (int32_t)pbw;
     f->pad_after[0] = (int32_t)pah; f->pad_after[1] = (int32_t)paw;
-    f->w_strides[0] = t.w_strides[1];        // per output channel within the group...
-    if (t.Cout_g == 1) f->w_strides[0] = t.w_strides[0];
-    f->w_strides[1] = t.w_strides[0];        // (one input channel: unused)
+    f->w_strides[0] = co_stride;
+    f->w_strides[1] = ci_stride;
     f->w_strides[2] = -t.w_strides[2];
     f->w_strides[3] = -t.w_strides[3];
     *q = p;

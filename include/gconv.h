@@ -278,10 +278,10 @@ gconv_status conv_grouped_forward(const gconv_desc *d, const void *x,
  * conv_transpose1d_bind (a forward desc is GCONV_ERR_KIND).  Pointers,
  * stream and errors as conv_dw_forward; w is [C_in, C_out/groups, KH, KW]
  * by the strides given to the bind.  A stride-1 transposed convolution
- * with one input channel per group is the forward convolution with the
- * kernel flipped and padding d*(K-1) - crop, and runs on the forward
- * schedules; the others run on dw_line (channels-last depthwise), or
- * grp_reduce / dw_flat. */
+ * with one input or one output channel per group is the forward convolution
+ * with the kernel flipped and padding d*(K-1) - crop, and runs on the
+ * forward schedules; the others run on dw_line (channels-last depthwise),
+ * or grp_reduce / dw_flat. */
 gconv_status conv_transpose_forward(const gconv_desc *d, const void *x, const void *w,
                                     const void *bias, void *y, gconv_stream stream);
 

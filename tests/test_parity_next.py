@@ -148,6 +148,8 @@ TR = [
     ("m3_3x3_s1", 1, 1, 3, 8, 7, 9, 3, 3, (1, 1), (1, 1), (1, 1), (0, 0), (1, 1)),
     ("g4x2_3x3_s2", 1, 4, 2, 4, 8, 8, 3, 3, (2, 2), (1, 1), (1, 1), (1, 1), (1, 1)),
     ("g8x8_5x5_s1", 1, 8, 8, 2, 9, 10, 5, 5, (1, 1), (2, 2), (2, 2), (0, 0), (1, 1)),
+    ("g4x1_3x3_s1", 2, 4, 1, 6, 9, 10, 3, 3, (1, 1), (1, 0), (1, 2), (0, 1), (1, 1)),
+    ("g8x1_4x2_s1_d2", 1, 8, 1, 3, 8, 7, 4, 2, (1, 1), (3, 1), (2, 0), (0, 0), (2, 1)),
 ]
 
 
