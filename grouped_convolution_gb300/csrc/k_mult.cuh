@@ -55,7 +55,8 @@ struct MultGeom {
     int shift;      // first window column minus the box's first column
     int spr;        // 4-column slots per band row
     int BWX;        // box width (elements, multiple of 16 bytes)
-    int pitch;      // fp32 elements per band row (multiple of 4)
+    int pitch;      // columns per band row (multiple of 4)
+    int rstride;    // fp32 elements per band row in shared memory (columns + padding)
     int stage;      // bytes per raw stage (multiple of 128)
     int band_off;   // byte offsets in shared memory
     int w_off;
@@ -67,6 +68,13 @@ struct MultGeom {
     int use_tma;    // x is described by a tensor map
     int vec_store;  // rows of y allow 16-byte stores of S pixels
 };
+
+// With 8 pixels per thread at column stride 1, neighbouring threads' windows
+// start 32 bytes apart, so a quarter-warp's 16-byte loads hit each bank twice.
+// Four padding floats after every 8 columns (column c at c + (c / 8) * 4)
+// put the 8 window starts of a quarter-warp on 8 different bank quads.
+constexpr bool mult_pad(int S, int SW) { return S == 8 && SW == 1; }
+__host__ __device__ constexpr int mult_col(int c, bool pad) { return pad ? c + (c >> 3) * 4 : c; }
 
 // 16-byte shared loads of a thread's window (KW = 0: any width up to 9).
 template <int S, int SW, int KW>
@@ -103,10 +111,11 @@ inline bool mult_band(const Params &p, int es, int CC, int tr_cap, MultGeom &g) 
     const int wl4 = ((g.S - 1) * p.sw + kMultMaxKW + 3) / 4;
     const int span = (g.PGn - 1) * g.S * p.sw + 4 * wl4;
     g.pitch = 4 * g.spr > span ? 4 * g.spr : (span + 3) / 4 * 4;
+    g.rstride = mult_pad(g.S, p.sw) ? g.pitch + ((g.pitch + 7) >> 3) * 4 : g.pitch;
     g.box_bytes = g.rows_in * g.BWX * es;
     g.stage = (g.box_bytes + 127) / 128 * 128;
     g.band_off = 2 * g.stage;
-    g.w_off = g.band_off + 2 * g.rows_in * g.pitch * 4;
+    g.w_off = g.band_off + 2 * g.rows_in * g.rstride * 4;
     g.bar_off = g.w_off + ((p.KH * p.KW * g.m + g.m) * 4 + 15) / 16 * 16;
     g.smem = g.bar_off + 32;   // two mbarriers, failure flag
     return g.smem <= kMultSmemCap;
@@ -215,11 +224,13 @@ __device__ __forceinline__ void mult_block(const float *brow, int pitch, int nq,
     }
     for (int qq = 0; qq < nq; ++qq) {
         // Input row qq of this thread's rows, read once for both output rows.
-        const float4 *src = reinterpret_cast<const float4 *>(brow + qq * pitch);
+        const float *src = brow + qq * pitch;
         float xr[WL4 * 4];
 #pragma unroll
         for (int l = 0; l < WL4; ++l) {
-            const float4 v = src[l];
+            // columns 4l .. 4l+3 of the window (the window starts on a
+            // multiple of 8 columns when the band is padded)
+            const float4 v = *reinterpret_cast<const float4 *>(src + mult_col(4 * l, mult_pad(S, SW)));
             xr[4 * l] = v.x; xr[4 * l + 1] = v.y; xr[4 * l + 2] = v.z; xr[4 * l + 3] = v.w;
         }
 #pragma unroll
@@ -285,7 +296,8 @@ mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     const uint32_t bars = ring + (uint32_t)g.bar_off;
     volatile int *failed = reinterpret_cast<volatile int *>(mult_smem + g.bar_off + 16);
     const int KW = KWT ? KWT : p.KW;
-    const int band_floats = g.rows_in * g.pitch;
+    const int band_floats = g.rows_in * g.rstride;
+    constexpr bool PAD = mult_pad(S, SW);
 
     const int t = threadIdx.x;
     const int per = g.items / g.ctas, extra = g.items % g.ctas;
@@ -328,7 +340,7 @@ mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
         int r = slot_r0, f = slot_f0;
         while (r < g.rows_in) {
             const T *src = raw + r * g.BWX + 4 * f;
-            *reinterpret_cast<float4 *>(band + r * g.pitch + 4 * f) =
+            *reinterpret_cast<float4 *>(band + r * g.rstride + mult_col(4 * f, PAD)) =
                 make_float4(Elem<T>::to_f32(src[0]), Elem<T>::to_f32(src[1]),
                             Elem<T>::to_f32(src[2]), Elem<T>::to_f32(src[3]));
             f += slot_df;
@@ -357,7 +369,7 @@ mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
 
     const int trow = t / g.PGn, pg = t - trow * g.PGn;
     const bool thread_on = trow < g.TR;
-    const int brow_off = trow * kMultRT * p.sh * g.pitch + pg * S * SW;
+    const int brow_off = trow * kMultRT * p.sh * g.rstride + mult_col(pg * S * SW, PAD);
     const int nq = (kMultRT - 1) * p.sh + p.KH;       // band rows a thread reads
 
     int cur_c = -1;
@@ -410,7 +422,7 @@ mult_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             const bool full = g.vec_store && ow0 + S <= p.OW;
             const int rows = p.OH - oh0 < kMultRT ? p.OH - oh0 : kMultRT;
             for (int mb = 0; mb < g.m; mb += MB)
-                mult_block<T, SW, MB, KWT>(band + brow_off, g.pitch, nq, p.sh, p.KH, KW, wsm + mb,
+                mult_block<T, SW, MB, KWT>(band + brow_off, g.rstride, nq, p.sh, p.KH, KW, wsm + mb,
                                            g.m, bsm + mb, ybase + (int64_t)mb * p.ys[1], p.ys[1],
                                            p.ys[2], rows, full, p.OW - ow0, bad);
         }
