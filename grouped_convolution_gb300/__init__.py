@@ -31,6 +31,7 @@ __all__ = [
     "conv1d_bind", "conv_transpose_bind", "conv_transpose1d_bind", "conv_transpose_forward",
     "grad_input_shape_and_stride", "conv_backward_input", "conv_backward_weight_workspace_size",
     "conv_backward_weight", "conv_backward_weight_noalloc", "conv_backward_weight_noalloc_limit",
+    "conv_autotune", "conv_autotune_clear",
     "conv1d", "conv_transpose2d", "conv_transpose1d",
     "conv2d_backward", "GconvError", "SCHEDULES", "lib_path",
 ]
@@ -120,6 +121,11 @@ def _load():
         lib.conv_backward_weight_workspace_size.argtypes = [P(Desc), P(ctypes.c_uint64)]
         lib.conv_backward_weight.restype = i32
         lib.conv_backward_weight.argtypes = [P(Desc), vp, vp, vp, vp, vp, ctypes.c_uint64, vp]
+        lib.conv_autotune.restype = i32
+        lib.conv_autotune.argtypes = [P(Desc), vp, vp, vp, vp, vp, i32, P(i32),
+                                      P(ctypes.c_float)]
+        lib.conv_autotune_clear.restype = None
+        lib.conv_autotune_clear.argtypes = []
         lib.conv_backward_weight_noalloc.restype = i32
         lib.conv_backward_weight_noalloc.argtypes = [P(Desc), vp, vp, vp, vp, vp]
         lib.conv_backward_weight_noalloc_limit.restype = ctypes.c_uint64
@@ -366,6 +372,21 @@ def conv_backward_weight_noalloc(desc: Desc, x, gy, dw, db, stream=None):
 def conv_backward_weight_noalloc_limit() -> int:
     """Bytes of the fixed scratch buffer conv_backward_weight_noalloc uses."""
     return int(_load().conv_backward_weight_noalloc_limit())
+
+
+def conv_autotune(desc: Desc, x, w, bias, y, reps: int = 10, stream=None):
+    """Time every schedule that takes this call and record the fastest for
+    its shape; returns (schedule name, microseconds per launch)."""
+    sch = ctypes.c_int32()
+    us = ctypes.c_float()
+    _check(_load().conv_autotune(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
+                                 _stream_ptr(stream), int(reps), ctypes.byref(sch),
+                                 ctypes.byref(us)), "conv_autotune")
+    return conv_schedule_name(sch.value), float(us.value)
+
+
+def conv_autotune_clear() -> None:
+    _load().conv_autotune_clear()
 
 
 def conv_select_schedule(desc: Desc, x, w, bias, y) -> str:

@@ -15,6 +15,9 @@
 #include <climits>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <vector>
 
 #include "gconv_internal.h"
 
@@ -496,8 +499,48 @@ static bool flipped_forward(const gconv_desc &t, const Ptrs &p, gconv_desc *f, P
     return true;
 }
 
+// Schedules chosen by conv_autotune, per call shape: every desc field that
+// shapes the launch, and the pointers' alignment (which decides what the
+// vectorised schedules take).
+static std::mutex g_tuned_mutex;
+static std::map<std::vector<int64_t>, int32_t> g_tuned;
+
+static std::vector<int64_t> tune_key(const gconv_desc &d, const Ptrs &p) {
+    std::vector<int64_t> k = {d.dtype, d.layout, d.transposed, d.spatial_dims, d.has_bias,
+                              d.unbatched, d.N, d.C_in, d.H, d.W, d.C_out, d.groups, d.KH, d.KW,
+                              d.stride[0], d.stride[1], d.pad_before[0], d.pad_before[1],
+                              d.pad_after[0], d.pad_after[1], d.dilation[0], d.dilation[1],
+                              d.output_padding[0], d.output_padding[1], d.b_stride};
+    for (int i = 0; i < 4; ++i) {
+        k.push_back(d.x_strides[i]);
+        k.push_back(d.w_strides[i]);
+        k.push_back(d.y_strides[i]);
+    }
+    const void *ptrs[4] = {p.x, p.w, p.b, p.y};
+    for (const void *q : ptrs) k.push_back((int64_t)(reinterpret_cast<uintptr_t>(q) & 127));
+    return k;
+}
+
+static int32_t tuned_schedule(const gconv_desc &d, const Ptrs &p) {
+    std::lock_guard<std::mutex> lock(g_tuned_mutex);
+    if (g_tuned.empty()) return GCONV_SCHED_AUTO;
+    auto it = g_tuned.find(tune_key(d, p));
+    return it == g_tuned.end() ? GCONV_SCHED_AUTO : it->second;
+}
+
+static gconv_status plan_with(const gconv_desc &d, const Ptrs &p, int32_t req, Plan *out);
+
 static gconv_status plan_call(const gconv_desc &d, const Ptrs &p, Plan *out) {
-    const int32_t req = requested_schedule(d);
+    int32_t req = requested_schedule(d);
+    if (req == GCONV_SCHED_AUTO) {
+        // A schedule timed for this shape wins while it still takes the call.
+        const int32_t tuned = tuned_schedule(d, p);
+        if (tuned != GCONV_SCHED_AUTO && plan_with(d, p, tuned, out) == GCONV_OK) return GCONV_OK;
+    }
+    return plan_with(d, p, req, out);
+}
+
+static gconv_status plan_with(const gconv_desc &d, const Ptrs &p, int32_t req, Plan *out) {
     if (d.transposed) {
         gconv_desc f;
         Ptrs q;
@@ -581,6 +624,72 @@ gconv_status conv_transpose_forward(const gconv_desc *d, const void *x, const vo
                                     const void *bias, void *y, gconv_stream stream) {
     if (d && d->magic == kDescMagic && !d->transposed) return GCONV_ERR_KIND;
     return run(d, x, w, bias, y, stream);
+}
+
+gconv_status conv_autotune(const gconv_desc *d, const void *x, const void *w, const void *bias,
+                           void *y, gconv_stream stream, int32_t reps, int32_t *schedule,
+                           float *us) {
+    if (reps < 1) return GCONV_ERR_SHAPE;
+    gconv_status st = check_call(d, x, w, bias, y);
+    if (st != GCONV_OK) return st;
+    const Ptrs p{x, w, bias, y};
+    if (empty_problem(d)) {
+        if (schedule) *schedule = pick(*d, p);
+        if (us) *us = 0.f;
+        return GCONV_OK;
+    }
+    st = take_injected();
+    if (st != GCONV_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t ce = cudaEventCreate(&e0);
+    if (ce == cudaSuccess) ce = cudaEventCreate(&e1);
+    int32_t best = GCONV_SCHED_AUTO;
+    float best_ms = 0.f;
+    for (int32_t sch = 0; sch < GCONV_SCHED_COUNT && ce == cudaSuccess; ++sch) {
+        Plan pl;
+        if (plan_with(*d, p, sch, &pl) != GCONV_OK || pl.schedule != sch) continue;
+        const Params pr = make_params(pl.d);
+        int launches = 0;
+        ce = kSchedules[sch]->launch(pr, pl.p, s, &launches);   // warm-up
+        g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
+        if (ce == cudaSuccess) ce = cudaEventRecord(e0, s);
+        for (int32_t r = 0; r < reps && ce == cudaSuccess; ++r) {
+            ce = kSchedules[sch]->launch(pr, pl.p, s, &launches);
+            g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
+        }
+        if (ce == cudaSuccess) ce = cudaEventRecord(e1, s);
+        if (ce == cudaSuccess) ce = cudaEventSynchronize(e1);
+        float ms = 0.f;
+        if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, e0, e1);
+        if (ce == cudaSuccess && (best == GCONV_SCHED_AUTO || ms < best_ms)) {
+            best = sch;
+            best_ms = ms;
+        }
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    if (ce != cudaSuccess) return after_launch(ce, 0);
+    if (best == GCONV_SCHED_AUTO) return GCONV_ERR_SCHEDULE;   // nothing takes the call
+    {
+        std::lock_guard<std::mutex> lock(g_tuned_mutex);
+        g_tuned[tune_key(*d, p)] = best;
+    }
+    if (schedule) *schedule = best;
+    if (us) *us = best_ms * 1000.f / (float)reps;
+    // The last schedule timed wrote y; run the chosen one last so y holds
+    // its result.
+    Plan pl;
+    st = plan_with(*d, p, best, &pl);
+    if (st != GCONV_OK) return st;
+    int launches = 0;
+    ce = kSchedules[best]->launch(make_params(pl.d), pl.p, s, &launches);
+    return after_launch(ce, launches);
+}
+
+void conv_autotune_clear(void) {
+    std::lock_guard<std::mutex> lock(g_tuned_mutex);
+    g_tuned.clear();
 }
 
 // The transposed convolution that computes dx for a forward desc: input gy

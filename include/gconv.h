@@ -285,6 +285,25 @@ gconv_status conv_grouped_forward(const gconv_desc *d, const void *x,
 gconv_status conv_transpose_forward(const gconv_desc *d, const void *x, const void *w,
                                     const void *bias, void *y, gconv_stream stream);
 
+/* Timed schedule choice (PR #25085, second paragraph: the template's
+ * schedules are timed at compile time and the fastest is used).  Runs every
+ * schedule that takes this call (forward or transposed desc) once to warm
+ * up and then `reps` times on `stream`, times each with CUDA events, and
+ * records the fastest for the call's shape: later calls whose desc has
+ * GCONV_SCHED_AUTO (and no process-wide override) with the same shape,
+ * dtype, layout, strides and pointer alignment run it.  Unlike the other
+ * entry points it waits for the stream (to read the events) and creates
+ * and destroys two CUDA events; it writes y (the chosen schedule runs
+ * last, so y holds its result).  *schedule gets the choice and *us its
+ * time per launch in microseconds (either may be NULL).  reps < 1 is
+ * GCONV_ERR_SHAPE; the record is process-wide and guarded by a mutex. */
+gconv_status conv_autotune(const gconv_desc *d, const void *x, const void *w, const void *bias,
+                           void *y, gconv_stream stream, int32_t reps, int32_t *schedule,
+                           float *us);
+
+/* Forget every schedule conv_autotune recorded. */
+void conv_autotune_clear(void);
+
 /* Which schedule a forward call with this desc and these pointers would run
  * (the picker, or the forced schedule), without launching anything.  Pointer
  * values are only inspected for alignment.  Returns GCONV_ERR_SCHEDULE /
