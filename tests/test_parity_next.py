@@ -300,3 +300,96 @@ def test_every_new_path_ran():
     names = {k[1] for k in RAN}
     for want in ("dw_flat", "grp_reduce", "dw_line", "dw_row8"):
         assert want in names, (want, dict(RAN))
+
+
+# ------------------------------------------------- alignment and guard bands
+
+def _offset_copy(t, elems=1, pad=8):
+    """t copied into a buffer at an element offset (breaks 16-byte
+    alignment), keeping t's strides."""
+    n = t.untyped_storage().nbytes() // t.element_size()
+    buf = torch.empty(n + pad, dtype=t.dtype, device="cuda")
+    out = torch.as_strided(buf, t.shape, t.stride(), elems)
+    out.copy_(t.cuda())
+    return out
+
+
+@pytest.mark.parametrize("schedule", ["auto", "dw_line", "dw_flat", "grp_reduce"])
+def test_transposed_misaligned_input(schedule):
+    case = ("mis_up", 2, 1, 1, 32, 9, 11, 4, 4, (2, 2), (1, 1), (1, 1))
+    wl = wl_of(case, "bf16", True, True, 810, transposed=True)
+    x, w, b = make_inputs(wl)
+    xd = _offset_copy(x)
+    wd, bd = w.cuda(), b.cuda()
+    d = gc.bind(xd, wd, bd, wl.stride, wl.pad_before, wl.pad_after, 1, wl.groups, True, 0)
+    d.schedule = gc.SCHEDULES[schedule]
+    y = gc.empty_output(d, xd)
+    try:
+        name = gc.conv_select_schedule(d, xd, wd, bd, y)
+    except gc.GconvError as e:
+        assert schedule == "dw_line" and e.status == 7   # needs 16-byte alignment
+        return
+    assert name != "dw_line"
+    gc.run(d, xd, wd, bd, y)
+    torch.cuda.synchronize()
+    ref, bound = oracle.reference(wl, x, w, b)
+    check(y, ref, bound, "bf16")
+
+
+def test_backward_misaligned_and_guard_bands():
+    case = BWD[0]
+    wl, x, w, gy = bwd_inputs(case, "bf16", True, 820)
+    dev = torch.device("cuda")
+    xd, gyd, wd = _offset_copy(x), _offset_copy(gy), w.to(dev)
+    d = gc.conv_bind(xd, wd, None, wl.stride, wl.pad_before, wl.pad_after, 1, wl.groups)
+    g = oracle.conv2d_backward(x, w, gy, wl.stride, wl.pad_before, wl.pad_after, wl.groups)
+    pad = 2048
+    poison = torch.tensor(777.0).to(torch.bfloat16)
+    # dx into a guarded buffer
+    sizes, strides = gc.grad_input_shape_and_stride(d)
+    n = int(np.prod(sizes))
+    bufx = torch.full((n + 2 * pad,), 777.0, device=dev).to(torch.bfloat16)
+    dx = torch.as_strided(bufx, sizes, strides, pad)
+    gc.conv_backward_input(d, gyd, wd, dx)
+    # dw / db into guarded buffers; the misaligned x and gy take the generic form
+    nw = w.numel()
+    bufw = torch.full((nw + 2 * pad,), 777.0, device=dev).to(torch.bfloat16)
+    dw = torch.as_strided(bufw, tuple(w.shape), w.stride(), pad)
+    bufb = torch.full((d.C_out + 2 * pad,), 777.0, device=dev).to(torch.bfloat16)
+    db = torch.as_strided(bufb, (d.C_out,), (1,), pad)
+    nbytes = gc.conv_backward_weight_workspace_size(d)
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=dev)
+    gc.conv_backward_weight(d, xd, gyd, dw, db, ws, nbytes)
+    torch.cuda.synchronize()
+    for buf, m in ((bufx, n), (bufw, nw), (bufb, d.C_out)):
+        assert bool((buf[:pad] == poison).all()) and bool((buf[pad + m:] == poison).all())
+    check(dx, g["dx"][0], g["dx"][1], "bf16")
+    check(dw, g["dw"][0], g["dw"][1], "bf16")
+    check(db, g["db"][0], g["db"][1], "bf16")
+
+
+@pytest.mark.parametrize("kind", ["dilated", "causal_1d", "transposed"])
+def test_dw_line_output_guard_bands(kind):
+    if kind == "dilated":
+        wl = wl_of(DIL[0], "bf16", True, True, 830, dilation=DIL[0][12])
+    elif kind == "causal_1d":
+        wl = wl_of(ONED[0], "bf16", True, True, 831, spatial_dims=1)
+    else:
+        wl = wl_of(TR[0], "bf16", True, True, 832, transposed=True)
+    x, w, b = make_inputs(wl)
+    dev = torch.device("cuda")
+    xd, wd, bd = x.to(dev), w.to(dev), b.to(dev)
+    d = gc.bind(xd, wd, bd, wl.stride, wl.pad_before, wl.pad_after, wl.dilation, wl.groups,
+                wl.transposed, wl.output_padding)
+    d.schedule = gc.SCHEDULES["dw_line"]
+    sizes, strides = gc.out_shape_and_stride(d)
+    n = int(np.prod(sizes))
+    pad = 4096
+    buf = torch.full((n + 2 * pad,), 777.0, device=dev).to(torch.bfloat16)
+    y = torch.as_strided(buf, sizes, strides, pad)
+    gc.run(d, xd, wd, bd, y)
+    torch.cuda.synchronize()
+    poison = torch.tensor(777.0).to(torch.bfloat16)
+    assert bool((buf[:pad] == poison).all()) and bool((buf[pad + n:] == poison).all())
+    ref, bound = oracle.reference(wl, x, w, b)
+    check(y, ref, bound, "bf16")
