@@ -234,7 +234,7 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
                     // vectors, tap j and pixel i at slot j + i.
                     constexpr int NW = S + KWM - 1;
                     const int last = tab_p[2 * ph], cmin = tab_p[2 * ph + 1];
-                    const int nv = last < 0 ? 0 : last / p.sw + 1;
+                    const int nv = last < 0 ? 0 : (int)g.fd_ph.div((uint32_t)last) + 1;
                     float2 win[NW][P];
                     const int iw0 = q0 + cmin;
 #pragma unroll
@@ -251,17 +251,18 @@ line_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restric
                     }
 #pragma unroll
                     for (int j = 0; j < KWM; ++j) {
-                        if (j >= nv) break;
-                        const int kw = last - j * p.sw;
-                        float2 wk[P];
-                        const float2 *src = wv + ((kh * p.KW + kw) * cb) / 2;
+                        if (j < nv) {   // a guard, not a break: the loop stays unrolled
+                            const int kw = last - j * p.sw;
+                            float2 wk[P];
+                            const float2 *src = wv + ((kh * p.KW + kw) * cb) / 2;
 #pragma unroll
-                        for (int k = 0; k < P; ++k) wk[k] = src[k];
+                            for (int k = 0; k < P; ++k) wk[k] = src[k];
 #pragma unroll
-                        for (int i = 0; i < S; ++i)
+                            for (int i = 0; i < S; ++i)
 #pragma unroll
-                            for (int k = 0; k < P; ++k)
-                                fma2_packed(acc[i][k], wk[k], win[j + i][k]);
+                                for (int k = 0; k < P; ++k)
+                                    fma2_packed(acc[i][k], wk[k], win[j + i][k]);
+                        }
                     }
                     continue;
                 }

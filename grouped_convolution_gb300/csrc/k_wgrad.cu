@@ -408,9 +408,8 @@ wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__r
             const int iw0 = ow0 - p.pbw;
 #pragma unroll
             for (int kh = 0; kh < KHM; ++kh) {
-                if (kh >= p.KH) break;
                 const int ih = oh * p.sh - p.pbh + kh * p.dh;
-                if (ih < 0 || ih >= p.H) continue;
+                if (kh >= p.KH || ih < 0 || ih >= p.H) continue;   // guards keep it unrolled
                 const T *xr = xn + (int64_t)ih * p.xs[2];
                 float2 win[NW][PR];
 #pragma unroll
@@ -427,12 +426,13 @@ wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__r
                 }
 #pragma unroll
                 for (int kw = 0; kw < KWM; ++kw) {
-                    if (kw >= p.KW) break;
+                    if (kw < p.KW) {
 #pragma unroll
-                    for (int i = 0; i < S; ++i)
+                        for (int i = 0; i < S; ++i)
 #pragma unroll
-                        for (int k = 0; k < PR; ++k)
-                            fma2_packed(acc[kh][kw][k], g[i][k], win[i + kw][k]);
+                            for (int k = 0; k < PR; ++k)
+                                fma2_packed(acc[kh][kw][k], g[i][k], win[i + kw][k]);
+                    }
                 }
             }
         }
