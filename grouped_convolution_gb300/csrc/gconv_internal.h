@@ -67,6 +67,14 @@ uint64_t wgrad_workspace_bytes(const Params &p);
 cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *dw, void *db,
                          void *workspace, cudaStream_t s, int *launches);
 
+// Its partial pass on the dw_row8 row ring (k_wgrad_row.cu), for channels-last
+// depthwise 3x3 calls at square stride 1 or 2: the workspace slices it writes
+// (0 when the shape is not taken), its pointer condition, and the launch.
+int wgrad_row_slices(const Params &p);
+bool wgrad_row_pointers(const void *x, const void *gy);
+cudaError_t wgrad_row_partial(const Params &p, const void *x, const void *gy, float *ws,
+                              cudaStream_t s);
+
 inline bool aligned(const void *p, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }

@@ -8,12 +8,16 @@
 // Two launches.  The first splits the output pixels (n, oh, ow) into slices
 // and writes one fp32 partial sum per (slice, co, tap) -- bias as one more
 // tap -- into the caller's workspace [slice][C_out][Cin_g*KH*KW + 1]; the
-// second adds each entry's slices in fp64 in a fixed order (eight
-// interleaved runs of slices, then the eight run sums) and rounds once into
-// dw (dense [C_out, Cin_g, KH, KW]) and db.  No atomics: the result is the
-// same on every run.
+// second adds each entry's slices (compensated fp32, as accurate as twice
+// the precision) in a fixed order (32 interleaved runs of slices, then a
+// fixed tree over the run sums) and rounds once into dw (dense
+// [C_out, Cin_g, KH, KW]) and db.  No atomics: the result is the same on
+// every run.
 //
-// Partial pass, three forms:
+// Partial pass, four forms:
+//  - channels-last depthwise 3x3 at square stride 1 or 2 (dilation 1): the
+//    forward's TMA row ring with x and gy rows staged together
+//    (k_wgrad_row.cu);
 //  - channels-last depthwise (one input and one output channel per group):
 //    a block owns a chunk of channel vectors and a slice of pixels; lane
 //    (cv, pixel lane) keeps CH channels x every tap in fp32 registers, walks
@@ -21,9 +25,9 @@
 //    input are loaded first, so they are in flight together, then packed
 //    FMAs), and the block adds its pixel lanes in shared memory, one tap at a
 //    time in a fixed order;
-//  - the same at column stride 1 with kernels of at most 3 x 3 (or 1 x 9):
-//    strips of 4 outputs that share one register window of inputs per
-//    kernel row (wgrad_strip_kernel);
+//  - the same with kernels of at most 3 x 3 (or 1 x 9) at column stride 1
+//    (any dilation) or 2 (dilation 1): strips of 4 outputs that share one
+//    register window of inputs per kernel row (wgrad_strip_kernel);
 //  - any other layout or group shape: a block owns (slice, co), every thread
 //    sums a tap over its pixels through the strides, and a fixed-order block
 //    reduction (shuffles, then shared memory) gives the slice's value.
@@ -54,6 +58,7 @@ struct WgPlan {
     FastDiv fd_ow, fd_oh;   // pixel index -> (n, oh, ow) when P < 2^32
     // strip form: items (n, oh, column phase, strip of kWgS outputs)
     int strip;        // 0: per-pixel form; 33 or 19: strip form for KH<=3,KW<=3 / KH=1,KW<=9
+                      // at column stride 1; 233 or 219: the same at column stride 2
     int PH, NSW;
     int64_t items;
     FastDiv fd_nsw, fd_ph;
@@ -108,12 +113,17 @@ bool wg_cl_pointers(const Params &p, const void *x, const void *gy, int ch) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// The strip form takes channels-last depthwise calls at column stride 1 with
-// kernels of at most 3 x 3, or height 1 and width at most 9.
+// The strip form takes channels-last depthwise calls with kernels of at most
+// 3 x 3, or height 1 and width at most 9, at column stride 1 (any dilation)
+// or column stride 2 (column dilation 1).
 int strip_kind(const Params &p) {
-    if (!cl_shape(p) || p.sw != 1) return 0;
-    if (p.KH <= 3 && p.KW <= 3) return 33;
-    if (p.KH == 1 && p.KW <= 9) return 19;
+    if (!cl_shape(p)) return 0;
+    int base = 0;
+    if (p.KH <= 3 && p.KW <= 3) base = 33;
+    else if (p.KH == 1 && p.KW <= 9) base = 19;
+    if (!base) return 0;
+    if (p.sw == 1) return base;
+    if (p.sw == 2 && p.dw == 1) return 200 + base;   // stride 2: window of contiguous columns
     return 0;
 }
 
@@ -132,7 +142,7 @@ WgPlan plan_for(const Params &p, bool cl, int strip = 0) {
         w.chunks = (int)cdiv(cv, 32);
         w.CVb = (int)cdiv(cv, w.chunks);
         w.PL = kWgThreads / w.CVb;
-        w.PH = p.dw;
+        w.PH = strip > 200 ? 1 : p.dw;
         const int Q = (p.OW + w.PH - 1) / w.PH;
         w.NSW = (Q + kWgS - 1) / kWgS;
         w.items = (int64_t)p.N * p.OH * w.PH * w.NSW;
@@ -341,10 +351,12 @@ wgrad_generic_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *_
 // Strip form of the partial pass: lane (cv, strip lane) walks items
 // (n, oh, column phase ph, strip of kWgS outputs ow = (q0 + i)*d + ph).  Per
 // item it loads the strip's gy vectors once, and for each kernel row the
-// strip's window of kWgS + KW - 1 input vectors (output i at tap kw reads
-// slot i + kw), so a pixel costs 1 + KH*(kWgS + KW - 1)/kWgS vector loads
-// instead of 1 + KH*KW, all of a row in flight together.
-template <typename T, int KHM, int KWM>
+// strip's window of input vectors: at column stride 1, kWgS + KW - 1 of them
+// d apart (output i at tap kw reads slot i + kw); at column stride 2 (SW = 2,
+// dilation 1, one phase), 2*(kWgS - 1) + KW contiguous ones (output i at tap
+// kw reads slot 2i + kw).  A pixel then costs 1 + KH*(window)/kWgS vector
+// loads instead of 1 + KH*KW, all of a row in flight together.
+template <typename T, int KHM, int KWM, int SW>
 __global__ void __launch_bounds__(kWgThreads)
 wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__restrict__ ws,
                    Params p, WgPlan pl) {
@@ -353,10 +365,12 @@ wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__r
     constexpr int CH = 4;
     constexpr int PR = CH / 2;
     constexpr int S = kWgS;
-    constexpr int NW = S + KWM - 1;
+    constexpr int NW = (S - 1) * SW + KWM;
     using V = Vec<T, CH>;
     using IO = VecIO<CH * (int)sizeof(T)>;
     __shared__ float red[kWgThreads * CH];        // [pixel lane][block channel]
+    const int nw = (S - 1) * SW + p.KW;           // window slots in use
+    const int jstep = SW == 1 ? p.dw : 1;         // columns between slots
 
     const int t = threadIdx.x;
     const int cvl = t % pl.CVb, lp = t / pl.CVb;
@@ -405,7 +419,7 @@ wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__r
                 }
             }
             const T *xn = x + (int64_t)n * p.xs[0] + c0;
-            const int iw0 = ow0 - p.pbw;
+            const int iw0 = ow0 * SW - p.pbw;
 #pragma unroll
             for (int kh = 0; kh < KHM; ++kh) {
                 const int ih = oh * p.sh - p.pbh + kh * p.dh;
@@ -414,8 +428,8 @@ wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__r
                 float2 win[NW][PR];
 #pragma unroll
                 for (int j = 0; j < NW; ++j) {
-                    const int iw = iw0 + j * p.dw;
-                    if (j < S + p.KW - 1 && iw >= 0 && iw < p.W) {
+                    const int iw = iw0 + j * jstep;
+                    if (j < nw && iw >= 0 && iw < p.W) {
                         V v;
                         IO::load(v, xr + (int64_t)iw * p.xs[3]);
                         widen<T, CH>(v, win[j]);
@@ -431,7 +445,7 @@ wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__r
                         for (int i = 0; i < S; ++i)
 #pragma unroll
                             for (int k = 0; k < PR; ++k)
-                                fma2_packed(acc[kh][kw][k], g[i][k], win[i + kw][k]);
+                                fma2_packed(acc[kh][kw][k], g[i][k], win[i * SW + kw][k]);
                     }
                 }
             }
@@ -468,11 +482,39 @@ wgrad_strip_kernel(const T *__restrict__ x, const T *__restrict__ gy, float *__r
 }
 
 // Second pass: entry e = (co, tap) of the [C_out][T1] table is the sum of
-// its slices.  A block owns 32 entries (lanes) and its 8 warps take slices
-// g, g+8, g+16, ... (four loads in flight at a time), each adding in fp64
-// in slice order; warp 0 then adds the 8 warp sums in warp order.  The
-// order is fixed, so the result is the same on every run.
-constexpr int kFinEntries = 32, kFinGroups = 8;
+// its slices.  A block owns 8 consecutive entries (one 32-byte sector per
+// slice) and its 32 groups take slices g, g+32, g+64, ... (four loads in
+// flight at a time), each adding them in slice order; the 32 group sums are
+// then added pairwise in a fixed tree.  The order is fixed, so the result is
+// the same on every run.
+//
+// The sums are compensated fp32 (a rounded sum plus its running error): each
+// addition is Knuth's error-free TwoSum and the errors are added up, as in
+// the cascaded summation of Ogita, Rump and Oishi, "Accurate sum and dot
+// product" (SIAM J. Sci. Comput., 2005), which is as accurate as summing in
+// twice the precision and rounding once.  FP64 would give the same accuracy,
+// but its pipe on this GPU is far slower than the FP32 pipes.  The explicit
+// round-to-nearest intrinsics keep the compiler from merging or reordering
+// the additions.
+constexpr int kFinEntries = 8, kFinGroups = 32;
+
+struct Sum2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ void two_sum_add(Sum2 &acc, float v) {
+    const float s = __fadd_rn(acc.hi, v);
+    const float bb = __fsub_rn(s, acc.hi);
+    const float err = __fadd_rn(__fsub_rn(acc.hi, __fsub_rn(s, bb)), __fsub_rn(v, bb));
+    acc.hi = s;
+    acc.lo = __fadd_rn(acc.lo, err);
+}
+
+__device__ __forceinline__ void two_sum_merge(Sum2 &acc, const Sum2 &o) {
+    const float lo = __fadd_rn(acc.lo, o.lo);
+    two_sum_add(acc, o.hi);
+    acc.lo = __fadd_rn(acc.lo, lo);
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kFinEntries * kFinGroups)
@@ -480,11 +522,11 @@ wgrad_finish_kernel(const float *__restrict__ ws, T *__restrict__ dw, T *__restr
                     int C_out, int T1, int slices) {
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ double part[kFinGroups][kFinEntries];
+    __shared__ Sum2 part[kFinGroups][kFinEntries];
     const int lane = threadIdx.x % kFinEntries, grp = threadIdx.x / kFinEntries;
     const int64_t total = (int64_t)C_out * T1;
     const int64_t e = (int64_t)blockIdx.x * kFinEntries + lane;
-    double s = 0.0;
+    Sum2 s{0.f, 0.f};
     if (e < total) {
         int sl = grp;
         for (; sl + 3 * kFinGroups < slices; sl += 4 * kFinGroups) {
@@ -492,24 +534,33 @@ wgrad_finish_kernel(const float *__restrict__ ws, T *__restrict__ dw, T *__restr
             const float b = ws[(int64_t)(sl + kFinGroups) * total + e];
             const float c = ws[(int64_t)(sl + 2 * kFinGroups) * total + e];
             const float d = ws[(int64_t)(sl + 3 * kFinGroups) * total + e];
-            s += (double)a;
-            s += (double)b;
-            s += (double)c;
-            s += (double)d;
+            two_sum_add(s, a);
+            two_sum_add(s, b);
+            two_sum_add(s, c);
+            two_sum_add(s, d);
         }
-        for (; sl < slices; sl += kFinGroups) s += (double)ws[(int64_t)sl * total + e];
+        for (; sl < slices; sl += kFinGroups) two_sum_add(s, ws[(int64_t)sl * total + e]);
     }
     part[grp][lane] = s;
     __syncthreads();
-    if (grp == 0 && e < total) {
-        double tot = 0.0;
 #pragma unroll
-        for (int g = 0; g < kFinGroups; ++g) tot += part[g][lane];
+    for (int h = kFinGroups / 2; h >= 1; h /= 2) {
+        if (grp < h) {
+            Sum2 m = part[grp][lane];
+            two_sum_merge(m, part[grp + h][lane]);
+            part[grp][lane] = m;
+        }
+        __syncthreads();
+    }
+    if (grp == 0 && e < total) {
+        const Sum2 tot = part[0][lane];
+        // An infinite sum leaves a NaN error term behind: keep the infinity.
+        const float v = isinf(tot.hi) ? tot.hi : __fadd_rn(tot.hi, tot.lo);
         const int co = (int)(e / T1), tap = (int)(e - (int64_t)co * T1);
         if (tap < T1 - 1)
-            dw[(int64_t)co * (T1 - 1) + tap] = from_f32<T>((float)tot);
+            dw[(int64_t)co * (T1 - 1) + tap] = from_f32<T>(v);
         else if (db)
-            db[co] = from_f32<T>((float)tot);
+            db[co] = from_f32<T>(v);
     }
 }
 
@@ -519,6 +570,20 @@ cudaError_t launch_cl(const Params &p, const T *x, const T *gy, float *ws, const
     constexpr int CH = wg_ch<T, TMAX>();
     return launch_pdl(wgrad_cl_kernel<T, TMAX, CH>, dim3(pl.slices, pl.chunks),
                       dim3(pl.CVb * pl.PL), 0, s, x, gy, ws, p, pl);
+}
+
+// The finish pass over `slices` partial slices of T1 entries per channel.
+cudaError_t finish_launch(const Params &p, const float *ws, void *dw, void *db, int T1,
+                          int slices, cudaStream_t s) {
+    const int64_t total = (int64_t)p.C_out * T1;
+    const int64_t blocks = (total + kFinEntries - 1) / kFinEntries;
+    if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+    return GCONV_DISPATCH_DTYPE(p.dtype, T, [&] {
+        cudaError_t e = launch_pdl(wgrad_finish_kernel<T>, dim3((unsigned)blocks),
+                                   dim3(kFinEntries * kFinGroups), 0, s, ws,
+                                   static_cast<T *>(dw), static_cast<T *>(db), p.C_out, T1, slices);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    });
 }
 
 }  // namespace
@@ -536,6 +601,8 @@ uint64_t wgrad_workspace_bytes(const Params &p) {
             if (st.slices > slices) slices = st.slices;
         }
     }
+    const int rs = wgrad_row_slices(p);
+    if (rs > slices) slices = rs;
     uint64_t b = (uint64_t)slices * (uint64_t)(p.C_out > 0 ? p.C_out : 0) * (uint64_t)g.T1 * 4u;
     return b < 16 ? 16 : b;
 }
@@ -543,6 +610,14 @@ uint64_t wgrad_workspace_bytes(const Params &p) {
 cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *dw, void *db,
                          void *workspace, cudaStream_t s, int *launches) {
     *launches = 2;
+    float *ws = static_cast<float *>(workspace);
+    const int rs = wgrad_row_slices(p);
+    if (rs && wgrad_row_pointers(x, gy)) {
+        // Depthwise 3x3 on the row ring, then the same finish.
+        cudaError_t e = wgrad_row_partial(p, x, gy, ws, s);
+        if (e != cudaSuccess) return e;
+        return finish_launch(p, ws, dw, db, p.KH * p.KW + 1, rs, s);
+    }
     bool cl = cl_shape(p);
     if (cl) cl = wg_cl_pointers(p, x, gy, cl_ch(p, cl_tmax(p)));
     // The strip form (4-channel loads, items counted in 32 bits).
@@ -550,17 +625,19 @@ cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *d
     if (sk && !(wg_cl_pointers(p, x, gy, 4) && (int64_t)p.N * p.OH * p.OW < 0xFFFFFFFFll))
         sk = 0;
     const WgPlan pl = plan_for(p, cl, sk);
-    float *ws = static_cast<float *>(workspace);
     return GCONV_DISPATCH_DTYPE(p.dtype, T, [&] {
         const T *xt = static_cast<const T *>(x);
         const T *gt = static_cast<const T *>(gy);
         cudaError_t e;
+        const dim3 sg(pl.slices, pl.chunks), sb(pl.CVb * pl.PL);
         if (sk == 33) {
-            e = launch_pdl(wgrad_strip_kernel<T, 3, 3>, dim3(pl.slices, pl.chunks),
-                           dim3(pl.CVb * pl.PL), 0, s, xt, gt, ws, p, pl);
+            e = launch_pdl(wgrad_strip_kernel<T, 3, 3, 1>, sg, sb, 0, s, xt, gt, ws, p, pl);
         } else if (sk == 19) {
-            e = launch_pdl(wgrad_strip_kernel<T, 1, 9>, dim3(pl.slices, pl.chunks),
-                           dim3(pl.CVb * pl.PL), 0, s, xt, gt, ws, p, pl);
+            e = launch_pdl(wgrad_strip_kernel<T, 1, 9, 1>, sg, sb, 0, s, xt, gt, ws, p, pl);
+        } else if (sk == 233) {
+            e = launch_pdl(wgrad_strip_kernel<T, 3, 3, 2>, sg, sb, 0, s, xt, gt, ws, p, pl);
+        } else if (sk == 219) {
+            e = launch_pdl(wgrad_strip_kernel<T, 1, 9, 2>, sg, sb, 0, s, xt, gt, ws, p, pl);
         } else if (cl) {
             if (pl.tmax == 9) e = launch_cl<T, 9>(p, xt, gt, ws, pl, s);
             else if (pl.tmax == 25) e = launch_cl<T, 25>(p, xt, gt, ws, pl, s);
@@ -571,13 +648,7 @@ cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *d
                            s, xt, gt, ws, p, pl);
         }
         if (e != cudaSuccess) return e;
-        const int64_t total = (int64_t)p.C_out * pl.T1;
-        const int64_t blocks = (total + kFinEntries - 1) / kFinEntries;
-        if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-        e = launch_pdl(wgrad_finish_kernel<T>, dim3((unsigned)blocks),
-                       dim3(kFinEntries * kFinGroups), 0, s, (const float *)ws,
-                       static_cast<T *>(dw), static_cast<T *>(db), p.C_out, pl.T1, pl.slices);
-        return e != cudaSuccess ? e : cudaGetLastError();
+        return finish_launch(p, ws, dw, db, pl.T1, pl.slices, s);
     });
 }
 

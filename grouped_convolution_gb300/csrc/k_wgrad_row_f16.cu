@@ -1,0 +1,11 @@
+// k_wgrad_row_f16.cu -- weight-gradient row-ring instantiations for __half (one
+// translation unit per dtype so the unrolled kernels compile in parallel).
+#include "k_wgrad_row.cuh"
+
+namespace gconv {
+int wrow_slices_f16(const Params &p) { return wrow_slices_dtype<__half>(p); }
+cudaError_t wrow_launch_f16(const Params &p, const void *x, const void *gy, float *ws,
+                         cudaStream_t s) {
+    return wrow_launch_dtype<__half>(p, x, gy, ws, s);
+}
+}  // namespace gconv

@@ -200,6 +200,16 @@ BWD = [
     ("dw1x7_s1", 2, 1, 1, 40, 5, 30, 1, 7, (1, 1), (0, 3), (0, 3), (1, 1)),
     ("dw2x2_s1_ragged", 3, 1, 1, 24, 7, 13, 2, 2, (2, 1), (0, 1), (1, 0), (1, 1)),
     ("dw1x3_d3", 1, 1, 1, 32, 4, 29, 1, 3, (1, 1), (0, 3), (0, 3), (1, 3)),
+    ("dw2x3_sw2_ragged", 2, 1, 1, 144, 6, 23, 2, 3, (1, 2), (1, 0), (0, 2), (1, 1)),
+    ("dw1x5_sw2", 2, 1, 1, 40, 3, 37, 1, 5, (1, 2), (0, 2), (0, 1), (1, 1)),
+    ("dw3_s2_d2", 1, 1, 1, 24, 11, 17, 3, 3, (2, 2), (2, 2), (2, 2), (2, 2)),
+    # long runs of output rows per CTA, both strides; two channel chunks
+    ("dw3_s1_tall", 8, 1, 1, 16, 160, 20, 3, 3, (1, 1), (1, 1), (1, 1), (1, 1)),
+    ("dw3_s2_tall", 8, 1, 1, 16, 161, 21, 3, 3, (2, 2), (1, 0), (0, 1), (1, 1)),
+    ("dw3_s1_c264", 1, 1, 1, 264, 6, 7, 3, 3, (1, 1), (1, 1), (1, 1), (1, 1)),
+    ("dw7_s1_tall", 4, 1, 1, 16, 70, 20, 7, 7, (1, 1), (3, 3), (3, 3), (1, 1)),
+    ("dw5_s2_tall", 4, 1, 1, 16, 81, 30, 5, 5, (2, 2), (2, 2), (2, 2), (1, 1)),
+    ("dw7_s2_ragged", 2, 1, 1, 24, 23, 19, 7, 7, (2, 2), (3, 2), (2, 3), (1, 1)),
 ]
 
 
