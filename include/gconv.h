@@ -114,8 +114,10 @@ typedef enum gconv_status {
 typedef enum gconv_schedule {
     GCONV_SCHED_AUTO = -1,
     GCONV_SCHED_DW_FLAT = 0,     /* fallback: any layout, multiplier and group shape */
-    GCONV_SCHED_DW_ROW8 = 1,     /* channels-last depthwise: 16-byte channel vectors,
-                                    register sliding window down the rows */
+    GCONV_SCHED_DW_ROW8 = 1,     /* channels-last depthwise, square 3/5/7 kernel, stride 1
+                                    or 2: input rows streamed through shared memory by TMA,
+                                    register sliding window down the rows; also the
+                                    stride-2 transposed form (a gather over the same ring) */
     GCONV_SCHED_DW_MULT = 2,     /* depthwise, multiplier <= 16: every output channel of an
                                     input channel from one input load */
     GCONV_SCHED_GRP_PLANE = 3,   /* grouped: a block per (image, group, tile), the group's

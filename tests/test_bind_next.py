@@ -15,7 +15,7 @@ import torch.nn.functional as F
 import grouped_convolution_gb300 as gc
 import oracle
 
-ERR = {"NULL": 1, "RANK": 2, "SHAPE": 4, "UNSUPPORTED": 5, "PADDING": 6, "SCHEDULE": 11,
+ERR = {"NULL": 1, "RANK": 2, "SHAPE": 4, "UNSUPPORTED": 5, "PADDING": 6, "ALIGN": 7, "SCHEDULE": 11,
        "KIND": 12, "WORKSPACE": 13}
 FAKE = 1 << 20
 
@@ -158,6 +158,25 @@ def test_schedule_selection_wider_envelope():
     assert select(d) == "dw_line"
     d.schedule = gc.SCHEDULES["dw_row8"]
     assert status_of(lambda: select(d)) == ERR["SCHEDULE"]
+    # stride 2 with a square 3/5/7 kernel: dw_row8's transposed ring (TMA
+    # needs a 16-byte aligned input)
+    for k in (3, 5, 7):
+        d = gc.conv_transpose_bind(cl4(8, 64, 20, 20), dense((64, 1, k, k)), None, 2, k // 2,
+                                   k // 2, 1, 1, 64, dtype="bfloat16")
+        assert select(d) == "dw_row8"
+        assert select(d, aligned=False) != "dw_row8"
+        d.schedule = gc.SCHEDULES["dw_row8"]
+        assert status_of(lambda: select(d, aligned=False)) == ERR["ALIGN"]
+    # ... but not at stride 3, with dilation, or in NCHW
+    d = gc.conv_transpose_bind(cl4(8, 64, 20, 20), dense((64, 1, 3, 3)), None, 3, 1, 1, 0, 1,
+                               64, dtype="bfloat16")
+    assert select(d) == "dw_line"
+    d = gc.conv_transpose_bind(cl4(8, 64, 20, 20), dense((64, 1, 3, 3)), None, 2, 2, 2, 1, 2,
+                               64, dtype="bfloat16")
+    assert select(d) == "dw_line"
+    d = gc.conv_transpose_bind(dense((8, 64, 20, 20)), dense((64, 1, 3, 3)), None, 2, 1, 1, 1, 1,
+                               64, dtype="bfloat16")
+    assert select(d) != "dw_row8"
 
 
 def test_kind_errors_and_dx_geometry():

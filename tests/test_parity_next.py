@@ -150,6 +150,12 @@ TR = [
     ("g8x8_5x5_s1", 1, 8, 8, 2, 9, 10, 5, 5, (1, 1), (2, 2), (2, 2), (0, 0), (1, 1)),
     ("g4x1_3x3_s1", 2, 4, 1, 6, 9, 10, 3, 3, (1, 1), (1, 0), (1, 2), (0, 1), (1, 1)),
     ("g8x1_4x2_s1_d2", 1, 8, 1, 3, 8, 7, 4, 2, (1, 1), (3, 1), (2, 0), (0, 0), (2, 1)),
+    # stride-2 depthwise square kernels: long runs, odd and even crops, two
+    # channel chunks, with and without bias
+    ("dw3_s2_tall", 4, 1, 1, 16, 40, 21, 3, 3, (2, 2), (0, 0), (0, 0), (0, 0), (1, 1)),
+    ("dw5_s2_odd", 2, 1, 1, 24, 17, 30, 5, 5, (2, 2), (1, 1), (2, 1), (1, 0), (1, 1)),
+    ("dw7_s2_c264", 1, 1, 1, 264, 6, 9, 7, 7, (2, 2), (3, 2), (2, 3), (1, 1), (1, 1)),
+    ("dw3_s2_c264", 2, 1, 1, 264, 9, 8, 3, 3, (2, 2), (1, 1), (1, 1), (1, 1), (1, 1)),
 ]
 
 
