@@ -51,7 +51,8 @@ struct RowTGeom {
     int pitch;       // bytes per staged pixel
     int box_bytes;   // bytes one row copy delivers
     int stage;       // bytes per stage (rounded up to 128)
-    int NS;          // stages
+    int NS;          // stages (a power of two)
+    int ns_log2;
     int units, ctas;
 };
 
@@ -107,10 +108,16 @@ bool rowt_geometry(const Params &p, RowTGeom &g) {
     g.pitch = g.CVc * VB;
     g.box_bytes = g.Wq * g.pitch;
     g.stage = (g.box_bytes + 127) / 128 * 128;
-    int ns = (200 * 1024 / row8_ctas_per_sm(K) - 8 * kRow8MaxStages - 16) / g.stage;
-    if (ns > kRow8MaxStages) ns = kRow8MaxStages;
+    // A power of two, so slots and phases come from masks and shifts.
+    const int fit = (200 * 1024 / row8_ctas_per_sm(K) - 8 * kRow8MaxStages - 16) / g.stage;
+    int ns = kRow8MaxStages, l2 = 3;
+    while (ns > fit) {
+        ns >>= 1;
+        --l2;
+    }
     if (ns < (K + 1) / 2 + 2) return false;
     g.NS = ns;
+    g.ns_log2 = l2;
     const int64_t units = (int64_t)p.N * g.CC * g.HC * p.OH;
     if (units > INT32_MAX / 2) return false;
     g.units = (int)units;
@@ -156,7 +163,7 @@ row8t_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     bool pdone = false;
     auto issue = [&]() {
         if (pdone) return;
-        const int slot = pissued % g.NS;
+        const int slot = pissued & (g.NS - 1);
         const uint32_t bar = bars + 8u * (uint32_t)slot;
         mbar_arrive_expect_tx(bar, (uint32_t)g.box_bytes);
         tma_load_4d(ring + (uint32_t)(slot * g.stage), &xmap, bar, prun.hc * g.CVc * VEC,
@@ -220,6 +227,7 @@ row8t_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         const int iw0 = run.cc * g.OWc - g.sh0 + pg * S;
         T *yn = y + (int64_t)run.n * p.ys[0] + (active ? c0 : 0);
         const int oh_end = run.oh0 + run.rows;
+        const bool cols_full = iw0 >= 0 && iw0 + S <= p.OW;   // no column check needed
         // Output rows in pairs (r, r + 1) with r + pad even: row r takes the
         // even taps kh = 2a and row r + 1 the odd taps kh = 2a + 1, both from
         // input row m - a (m = (r + pad)/2), so each input row's window is
@@ -230,8 +238,8 @@ row8t_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
             const int need = cbase + (m - run.j0) + 1;
             while (cnext < need) {
                 if (!bad) {
-                    if (mbar_wait(bars + 8u * (uint32_t)(cnext % g.NS),
-                                  (uint32_t)((cnext / g.NS) & 1), abort_flag)) {
+                    if (mbar_wait(bars + 8u * (uint32_t)(cnext & (g.NS - 1)),
+                                  (uint32_t)((cnext >> g.ns_log2) & 1), abort_flag)) {
                         ++cseen;
                     } else {
                         bad = true;
@@ -251,7 +259,7 @@ row8t_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
 #pragma unroll
             for (int a = 0; a <= KE / 2; ++a) {
                 const int seq = cbase + (m - a - run.j0);
-                const uint32_t st = ring + (uint32_t)((seq % g.NS) * g.stage) + win_off;
+                const uint32_t st = ring + (uint32_t)((seq & (g.NS - 1)) * g.stage) + win_off;
                 float2 xr[WIN][P];
 #pragma unroll
                 for (int q = 0; q < WIN; ++q) {
@@ -286,12 +294,18 @@ row8t_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                 for (int h = 0; h < 2; ++h) {
                     const int oh = r + h;
                     if (oh < run.oh0 || oh >= oh_end) continue;
-                    T *yrow = yn + (int64_t)oh * p.ys[2];
+                    T *yrow = yn + (int64_t)oh * p.ys[2] + (int64_t)iw0 * p.ys[3];
+                    if (cols_full) {
 #pragma unroll
-                    for (int i = 0; i < S; ++i) {
-                        const int iw = iw0 + i;
-                        if (iw >= 0 && iw < p.OW)
-                            IO::store(yrow + (int64_t)iw * p.ys[3], pack_pairs<T, VEC>(acc[h][i]));
+                        for (int i = 0; i < S; ++i)
+                            IO::store(yrow + i * p.ys[3], pack_pairs<T, VEC>(acc[h][i]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < S; ++i) {
+                            const int iw = iw0 + i;
+                            if (iw >= 0 && iw < p.OW)
+                                IO::store(yrow + i * p.ys[3], pack_pairs<T, VEC>(acc[h][i]));
+                        }
                     }
                 }
             }
@@ -314,7 +328,7 @@ row8t_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     // landing in this CTA's shared memory: wait for each once more (bounded).
     if (t == 0 && *abort_flag)
         for (int q = cseen; q < pissued; ++q)
-            (void)mbar_wait(bars + 8u * (uint32_t)(q % g.NS), (uint32_t)((q / g.NS) & 1));
+            (void)mbar_wait(bars + 8u * (uint32_t)(q & (g.NS - 1)), (uint32_t)((q >> g.ns_log2) & 1));
 }
 
 template <typename T, int K>
