@@ -39,6 +39,13 @@ namespace gconv {
 
 constexpr int kRowTS = 4;   // output columns per thread (even)
 
+// CTA size cap and persistent CTAs per SM.  3x3, measured on six shapes:
+// four 128-thread CTAs per SM beat two of 256 by 4-11 % and three of 160
+// (more CTAs overlap one another's per-pair barriers); 5x5 and 7x7 keep the
+// forward's shape.
+constexpr int rowt_max_threads(int K) { return K == 3 ? 128 : row8_max_threads(K); }
+constexpr int rowt_ctas_per_sm(int K) { return K == 3 ? 4 : row8_ctas_per_sm(K); }
+
 constexpr int rowt_win(int K) { return (kRowTS + K - 2) / 2 + 1; }
 
 struct RowTGeom {
@@ -84,7 +91,7 @@ bool rowt_geometry(const Params &p, RowTGeom &g) {
     constexpr int VEC = row8_vec<T>(K);
     constexpr int S = kRowTS;
     constexpr int VB = VEC * (int)sizeof(T);
-    constexpr int MAXT = row8_max_threads(K);
+    constexpr int MAXT = rowt_max_threads(K);
     constexpr int WIN = rowt_win(K);
     if (p.C_out % VEC != 0) return false;
     const int CV = p.C_out / VEC;
@@ -109,7 +116,7 @@ bool rowt_geometry(const Params &p, RowTGeom &g) {
     g.box_bytes = g.Wq * g.pitch;
     g.stage = (g.box_bytes + 127) / 128 * 128;
     // A power of two, so slots and phases come from masks and shifts.
-    const int fit = (200 * 1024 / row8_ctas_per_sm(K) - 8 * kRow8MaxStages - 16) / g.stage;
+    const int fit = (200 * 1024 / rowt_ctas_per_sm(K) - 8 * kRow8MaxStages - 16) / g.stage;
     int ns = kRow8MaxStages, l2 = 3;
     while (ns > fit) {
         ns >>= 1;
@@ -121,13 +128,13 @@ bool rowt_geometry(const Params &p, RowTGeom &g) {
     const int64_t units = (int64_t)p.N * g.CC * g.HC * p.OH;
     if (units > INT32_MAX / 2) return false;
     g.units = (int)units;
-    const int cap = 152 * row8_ctas_per_sm(K);
+    const int cap = 152 * rowt_ctas_per_sm(K);
     g.ctas = g.units < cap ? g.units : cap;
     return true;
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(row8_max_threads(K), row8_ctas_per_sm(K))
+__global__ void __launch_bounds__(rowt_max_threads(K), rowt_ctas_per_sm(K))
 row8t_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
              const T *__restrict__ b, T *__restrict__ y, Params p, RowTGeom g) {
     pdl_launch_dependents();
