@@ -34,7 +34,12 @@ bool row8t_supports(const gconv_desc &d, const Ptrs &q) {
 
 bool row8_supports(const gconv_desc &d, const Ptrs &q) {
     if (d.transposed) return row8t_supports(d, q);
-    if (!plain_forward(d)) return false;                    // dilation 1, forward
+    // Dilation 1, or 2 in both dims for 3x3 kernels at stride 1 (at stride 2
+    // every other staged row and column would go unused).
+    const bool dil1 = d.dilation[0] == 1 && d.dilation[1] == 1;
+    const bool dil2 = d.dilation[0] == 2 && d.dilation[1] == 2 && d.KH == 3 && d.KW == 3 &&
+                      d.stride[0] == 1 && d.stride[1] == 1;
+    if (!dil1 && !dil2) return false;
     if (d.Cin_g != 1 || d.Cout_g != 1) return false;          // multiplier 1
     if (d.layout != GCONV_LAYOUT_NHWC) return false;          // channel-contiguous
     if (d.KH != d.KW) return false;

@@ -22,7 +22,9 @@
 //    the CTA's lifetime.  Each staged input row is widened once into a
 //    window of (S-1)*S_W + KW vectors (32-bit shared addressing) and
 //    multiplied (packed fma.rn.f32x2 over channel pairs) into every output
-//    row still open on it: R = ceil(KH / S_H)
+//    row still open on it: R = ceil(((KH - 1)*d + 1) / S_H) (d: dilation,
+//    1, or 2 for 3x3 kernels at stride 1; taps then read every d-th row and
+//    window slot)
 //    accumulator sets rotate through the output rows, with set indices fixed
 //    at compile time by unrolling the row loop over one rotation period.
 //  - Accumulators start at the bias (fp32); a finished output row is
@@ -126,7 +128,7 @@ template <> struct Lds<16> {
     }
 };
 
-template <typename T, int K, int SH>
+template <typename T, int K, int SH, int D>
 __global__ void __launch_bounds__(row8_max_threads(K), row8_ctas_per_sm(K))
 row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             const T *__restrict__ w, const T *__restrict__ b, T *__restrict__ y, Params p,
@@ -140,9 +142,10 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     constexpr int P = VEC / 2;                   // channel pairs per thread
     constexpr int S = row8_s(K);
     constexpr int VB = VEC * (int)sizeof(T);     // bytes per vector
-    constexpr int R = (K + SH - 1) / SH;         // output rows open at once
+    constexpr int KX = (K - 1) * D + 1;          // input rows (columns) one output spans
+    constexpr int R = (KX + SH - 1) / SH;        // output rows open at once
     constexpr int U = SH * R;                    // rotation period = input rows per stage
-    constexpr int WIN = (S - 1) * SW + K;        // input vectors per window
+    constexpr int WIN = (S - 1) * SW + KX;       // input vectors per window
     using V = Vec<T, VEC>;
     using IO = VecIO<VB>;
     extern __shared__ __align__(128) unsigned char row8_ring[];
@@ -185,7 +188,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             if (pnext_u >= o1) {
                 pdone = true;
             } else {
-                prun = row8_run_at<K, SH>(pnext_u, o1, p.OH, g.CC, g.HC);
+                prun = row8_run_at<KX, SH>(pnext_u, o1, p.OH, g.CC, g.HC);
                 pnext_u += prun.rows;
                 pst = 0;
                 pnst = (prun.nin + U - 1) / U;
@@ -236,7 +239,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     };
     // The first run's weights are fetched before the row stream starts:
     // issued behind it they would wait for it.
-    int loaded_hc = row8_run_at<K, SH>(o0, o1, p.OH, g.CC, g.HC).hc;
+    int loaded_hc = row8_run_at<KX, SH>(o0, o1, p.OH, g.CC, g.HC).hc;
     stage_weights(loaded_hc);
 
     if (t == 0) {
@@ -244,7 +247,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
         for (int i = 0; i < g.NS; ++i) mbar_init(bars + 8u * i, 1);
         *abort_flag = 0;
         fence_barrier_init();
-        prun = row8_run_at<K, SH>(o0, o1, p.OH, g.CC, g.HC);
+        prun = row8_run_at<KX, SH>(o0, o1, p.OH, g.CC, g.HC);
         pnext_u = o0 + prun.rows;
         pnst = (prun.nin + U - 1) / U;
         for (int i = 0; i < g.NS; ++i) issue();   // prologue: NS stages in flight
@@ -259,7 +262,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
     int cwaited = 0;      // boxes this thread has seen arrive
     int u = o0;
     while (u < o1) {
-        const Row8Run run = row8_run_at<K, SH>(u, o1, p.OH, g.CC, g.HC);
+        const Row8Run run = row8_run_at<KX, SH>(u, o1, p.OH, g.CC, g.HC);
         u += run.rows;
         const int c0 = (run.hc * g.CVc + cvl) * VEC;
         const bool active = c0 < p.C_out;
@@ -333,7 +336,7 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
                 }
 #pragma unroll
                 for (int kh = 0; kh < K; ++kh) {
-                    const int d = ph - kh;               // (r - kh) - r0
+                    const int d = ph - kh * D;           // (r - kh*D) - r0
                     if (fmod_pos(d, SH) != 0) continue;  // no output row has tap row kh here
                     const int set = fmod_pos(fdiv(d, SH), R);
 #pragma unroll
@@ -342,16 +345,16 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
                         for (int kw = 0; kw < K; ++kw)
 #pragma unroll
                             for (int k = 0; k < P; ++k)   // packed: half the issue slots
-                                fma2_packed(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw][k]);
+                                fma2_packed(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw * D][k]);
                 }
                 // The output row whose last tap row this was is done.
-                const int d = ph - (K - 1);
+                const int d = ph - (KX - 1);
                 if (fmod_pos(d, SH) == 0) {
                     const int set = fmod_pos(fdiv(d, SH), R);
-                    const int jn = r - (K - 1);          // SH * output row within the run
+                    const int jn = r - (KX - 1);         // SH * output row within the run
                     if (active && jn >= 0 && jn < run.rows * SH) {
                         // output row jn / SH = r0 / SH + (ph - K + 1) / SH
-                        T *yrow = ystage + (int64_t)fdiv(ph - (K - 1), SH) * p.ys[2];
+                        T *yrow = ystage + (int64_t)fdiv(ph - (KX - 1), SH) * p.ys[2];
 #pragma unroll
                         for (int i = 0; i < S; ++i)
                             if (pix_ok[i])
@@ -395,19 +398,20 @@ bool row8_geometry(const Params &p, Row8Geom &g) {
     g.HC = (CV + g.CVc - 1) / g.CVc;
     const int pg_max = MAXT / g.CVc;
     const int pg_need = (p.OW + S - 1) / S;
+    const int KX = (K - 1) * p.dw + 1;   // columns (rows: dh) one output spans
     // Split the columns evenly over the fewest chunks that fit the CTA and
     // keep each staged segment within the 256-pixel TMA box.
     int cc = (pg_need + pg_max - 1) / pg_max;
     for (;; ++cc) {
         const int pg = (pg_need + cc - 1) / cc;
-        if ((pg * S - 1) * p.sw + K <= 256) break;
+        if ((pg * S - 1) * p.sw + KX <= 256) break;
     }
     g.PG = (pg_need + cc - 1) / cc;
     g.OWc = g.PG * S;
     g.CC = (p.OW + g.OWc - 1) / g.OWc;
-    g.Win = (g.OWc - 1) * p.sw + K;
+    g.Win = (g.OWc - 1) * p.sw + KX;
     g.pitch = g.CVc * VB;
-    g.box_bytes = g.Win * g.pitch * row8_rows_per_stage(K, p.sh);
+    g.box_bytes = g.Win * g.pitch * row8_rows_per_stage((K - 1) * p.dh + 1, p.sh);
     g.stage = (g.box_bytes + 127) / 128 * 128;
     int ns = (200 * 1024 / row8_ctas_per_sm(K) - (K * K + 1) * g.CVc * VEC * 4) / g.stage;
     if (ns > kRow8MaxStages) ns = kRow8MaxStages;
@@ -421,7 +425,7 @@ bool row8_geometry(const Params &p, Row8Geom &g) {
     return true;
 }
 
-template <typename T, int K, int SH>
+template <typename T, int K, int SH, int D>
 cudaError_t row8_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
     constexpr int VEC = row8_vec<T>(K);
     Row8Geom g;
@@ -432,15 +436,15 @@ cudaError_t row8_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
     const uint64_t strides[3] = {(uint64_t)p.xs[3] * es, (uint64_t)p.xs[2] * es,
                                  (uint64_t)p.xs[0] * es};
     const uint32_t box[4] = {(uint32_t)(g.CVc * VEC), (uint32_t)g.Win,
-                             (uint32_t)row8_rows_per_stage(K, SH), 1u};
+                             (uint32_t)row8_rows_per_stage((K - 1) * D + 1, SH), 1u};
     CUtensorMap map;
     if (!tma_encode_4d(&map, tma_dtype<T>(), q.x, dims, strides, box)) return cudaErrorInvalidValue;
     const size_t smem = (size_t)g.NS * g.stage + 8 * (size_t)g.NS + 16 +
                         (size_t)(K * K + 1) * g.CVc * VEC * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(row8_kernel<T, K, SH>,
+    cudaError_t e = cudaFuncSetAttribute(row8_kernel<T, K, SH, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(row8_kernel<T, K, SH>, dim3(g.ctas), dim3(g.CVc * g.PG), smem, s, map,
+    e = launch_pdl(row8_kernel<T, K, SH, D>, dim3(g.ctas), dim3(g.CVc * g.PG), smem, s, map,
                    static_cast<const T *>(q.x), static_cast<const T *>(q.w),
                    static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -449,11 +453,12 @@ cudaError_t row8_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
 template <typename T>
 cudaError_t row8_launch_dtype(const Params &p, const Ptrs &q, cudaStream_t s) {
     const int K = p.KH, SH = p.sh;
-#define GCONV_ROW8_CASE(KK, SS) \
-    if (K == KK && SH == SS) return row8_launch_t<T, KK, SS>(p, q, s);
-    GCONV_ROW8_CASE(3, 1) GCONV_ROW8_CASE(3, 2)
-    GCONV_ROW8_CASE(5, 1) GCONV_ROW8_CASE(5, 2)
-    GCONV_ROW8_CASE(7, 1) GCONV_ROW8_CASE(7, 2)
+#define GCONV_ROW8_CASE(KK, SS, DD) \
+    if (K == KK && SH == SS && p.dh == DD) return row8_launch_t<T, KK, SS, DD>(p, q, s);
+    GCONV_ROW8_CASE(3, 1, 1) GCONV_ROW8_CASE(3, 2, 1)
+    GCONV_ROW8_CASE(5, 1, 1) GCONV_ROW8_CASE(5, 2, 1)
+    GCONV_ROW8_CASE(7, 1, 1) GCONV_ROW8_CASE(7, 2, 1)
+    GCONV_ROW8_CASE(3, 1, 2)
 #undef GCONV_ROW8_CASE
     return cudaErrorNotSupported;
 }

@@ -130,8 +130,19 @@ def select(desc, aligned=True):
 
 
 def test_schedule_selection_wider_envelope():
-    # dilated channels-last depthwise -> dw_line; NCHW dilated -> dw_flat / grp_reduce
+    # dilation 2, 3x3, stride 1, channels-last depthwise -> dw_row8 (its
+    # dilated ring); other dilated channels-last depthwise -> dw_line; NCHW
+    # dilated -> dw_flat / grp_reduce
     d = gc.conv_bind(cl4(8, 64, 20, 20), dense((64, 1, 3, 3)), None, 1, 2, 2, 2, 64,
+                     dtype="bfloat16")
+    assert select(d) == "dw_row8"
+    for st, dl in ((2, 2), (1, 3)):
+        d = gc.conv_bind(cl4(8, 64, 20, 20), dense((64, 1, 3, 3)), None, st, dl, dl, dl, 64,
+                         dtype="bfloat16")
+        assert select(d) == "dw_line"
+        d.schedule = gc.SCHEDULES["dw_row8"]
+        assert status_of(lambda: select(d)) == ERR["SCHEDULE"]
+    d = gc.conv_bind(cl4(8, 64, 20, 20), dense((64, 1, 5, 5)), None, 1, 4, 4, 2, 64,
                      dtype="bfloat16")
     assert select(d) == "dw_line"
     d = gc.conv_bind(dense((8, 64, 20, 20)), dense((64, 1, 3, 3)), None, 1, 2, 2, 2, 64,

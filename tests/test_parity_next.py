@@ -75,6 +75,10 @@ DIL = [
     ("m2_3x3_d2", 1, 1, 2, 16, 12, 12, 3, 3, (1, 1), (2, 2), (2, 2), (2, 2)),
     ("g4x8_3x3_d2", 1, 4, 8, 4, 14, 15, 3, 3, (1, 1), (2, 2), (2, 2), (2, 2)),
     ("dw9_d2", 1, 1, 1, 16, 20, 20, 9, 9, (1, 1), (8, 8), (8, 8), (2, 2)),
+    # dw_row8's dilated ring (3x3, dilation 2, stride 1): long runs with
+    # asymmetric pads, two channel chunks
+    ("dw3_d2_tall", 4, 1, 1, 16, 60, 21, 3, 3, (1, 1), (2, 1), (1, 2), (2, 2)),
+    ("dw3_d2_c264", 1, 1, 1, 264, 9, 10, 3, 3, (1, 1), (2, 2), (2, 2), (2, 2)),
 ]
 
 
