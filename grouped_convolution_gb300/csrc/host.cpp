@@ -394,7 +394,8 @@ gconv_status grad_input_shape_and_stride(const gconv_desc *d, int32_t *rank,
 // fallback schedule dw_flat takes everything else.  Grouped calls the
 // tensor cores can take (4 or 8 channels per group, channels-last 16-bit)
 // run there.  Channels-last depthwise calls outside dw_row8's reach (1-D,
-// non-square or larger kernels, dilation, transposed) run on dw_line.  Other
+// non-square or larger kernels, dilation other than 2 on a stride-1 3x3,
+// transposed calls other than stride 2) run on dw_line.  Other
 // calls with too few outputs to give every thread of the GPU its own (fewer
 // than 152 SMs x 512) and a long tap loop split the taps across lanes.
 static int32_t pick(const gconv_desc &d, const Ptrs &p) {
