@@ -347,8 +347,9 @@ gconv_status conv_backward_weight_workspace_size(const gconv_desc *d, uint64_t *
  * the output pixels in fp32 into `workspace` (at least the bytes
  * conv_backward_weight_workspace_size gives, 16-byte aligned, owned by the
  * caller and not read before it is written), then a pass that adds the
- * slices in fp64 in a fixed order and rounds once.  The result is
- * deterministic.  x and gy as for the forward and conv_backward_input. */
+ * slices in a fixed order (compensated fp32 sums, as accurate as twice the
+ * precision) and rounds once.  The result is deterministic.  x and gy as
+ * for the forward and conv_backward_input. */
 gconv_status conv_backward_weight(const gconv_desc *d, const void *x, const void *gy,
                                   void *dw, void *db, void *workspace,
                                   uint64_t workspace_bytes, gconv_stream stream);

@@ -228,6 +228,17 @@ def test_backward_weight_workspace_contract():
     assert status_of(lambda: gc.conv_backward_weight_workspace_size(tr)) == ERR["KIND"]
 
 
+def test_backward_weight_workspace_covers_the_row_ring():
+    # Channels-last depthwise square 3/5/7 kernels at stride 1 or 2 take the
+    # row-ring partial pass: one fp32 slice of C_out x (KH*KW + 1) per
+    # persistent CTA (two per SM for 3x3, one for 5x5 / 7x7, 152 SMs).
+    for C, H, K, s in ((144, 56, 3, 1), (144, 56, 3, 2), (96, 56, 7, 1), (24, 112, 5, 2)):
+        d = gc.conv_bind(cl4(32, C, H, H), dense((C, 1, K, K)), None, s, K // 2, K // 2, 1, C,
+                         dtype="bfloat16")
+        per_sm = 2 if K == 3 else 1
+        assert gc.conv_backward_weight_workspace_size(d) >= 152 * per_sm * C * (K * K + 1) * 4
+
+
 def test_injected_error_on_new_entry_points():
     lib = gc._load()
     tr = gc.conv_transpose_bind(cl4(2, 16, 9, 9), dense((16, 1, 3, 3)), None, 2, 1, 1, 0, 1,
