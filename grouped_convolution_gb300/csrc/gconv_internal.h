@@ -61,6 +61,9 @@ inline bool plain_forward(const gconv_desc &d) {
 // behind conv_launch_count and the error behind conv_last_cuda_error.
 void note_launches(int launches);
 void note_cuda_error(int32_t e);
+// conv_test_inject_launch_error's pending value: GCONV_ERR_CUDA (recording
+// the value as the last CUDA error) instead of launching, once.
+gconv_status take_injected();
 
 // Backward weight pass (k_wgrad.cu): workspace bytes, and the launches.
 uint64_t wgrad_workspace_bytes(const Params &p);

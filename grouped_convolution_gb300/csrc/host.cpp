@@ -120,6 +120,17 @@ void note_launches(int launches) {
 
 void note_cuda_error(int32_t e) { t_last_cuda_error = e; }
 
+// The injected-error hook of conv_test_inject_launch_error: a pending value
+// makes this call fail as a launch error would, without launching.
+gconv_status take_injected() {
+    int32_t inj = g_inject.exchange(0);
+    if (inj != 0) {
+        t_last_cuda_error = inj;
+        return GCONV_ERR_CUDA;
+    }
+    return GCONV_OK;
+}
+
 Params make_params(const gconv_desc &d) {
     Params p{};
     p.N = (int)d.N; p.C_in = (int)d.C_in; p.H = (int)d.H; p.W = (int)d.W;
@@ -572,16 +583,7 @@ gconv_status conv_select_schedule(const gconv_desc *d, const void *x, const void
     return GCONV_OK;
 }
 
-// The injected-error hook, then a CUDA error check after the launches.
-static gconv_status take_injected() {
-    int32_t inj = g_inject.exchange(0);
-    if (inj != 0) {
-        t_last_cuda_error = inj;
-        return GCONV_ERR_CUDA;
-    }
-    return GCONV_OK;
-}
-
+// A CUDA error check after the launches.
 static gconv_status after_launch(cudaError_t e, int launches) {
     g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
     if (e == cudaSuccess) e = cudaGetLastError();

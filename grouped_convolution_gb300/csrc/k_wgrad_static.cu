@@ -15,8 +15,11 @@
 // stand-in, not device memory), so the device address is looked up with
 // cudaGetSymbolAddress once per device, on the first call made with that
 // device current, and cached.  That first call should come before any stream
-// capture begins.  Nothing here allocates: no cudaMalloc, no cudaFree, no
-// allocating library routine.
+// capture begins.  The cached address stays valid for as long as the device's
+// primary context lives: do not reset the device (cudaDeviceReset) while the
+// library is in use, since a new context may place the array elsewhere.
+// Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library
+// routine.
 //
 // Every call shares the one buffer and leaves its contents behind.  The
 // partial pass writes every entry it later reads, so nothing has to start at
@@ -79,6 +82,8 @@ gconv_status conv_backward_weight_noalloc(const gconv_desc *d, const void *x, co
     if (has_pixels && (!x || !gy)) return GCONV_ERR_NULL;
     const Params pr = make_params(*d);
     if (wgrad_workspace_bytes(pr) > kWgradStaticBytes) return GCONV_ERR_SCRATCH_LIMIT;
+    const gconv_status inj = take_injected();
+    if (inj != GCONV_OK) return inj;
     void *scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);
     if (e == cudaSuccess) {

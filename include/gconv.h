@@ -252,8 +252,10 @@ gconv_status conv_transpose1d_bind(const gconv_tensor *x, const gconv_tensor *w,
 
 /* The output's rank, sizes and element strides (PR #25084, second paragraph:
  * one function decides the output layout and both the op and its shape-only
- * variant use it).  OH = floor((H + pad_before_h + pad_after_h - KH) /
- * stride_h) + 1 and likewise OW; y is dense in the layout of x
+ * variant use it).  Forward: OH = floor((H + pad_before_h + pad_after_h -
+ * dilation_h * (KH - 1) - 1) / stride_h) + 1 and likewise OW (with
+ * dilation 1: floor((H + pad_before_h + pad_after_h - KH) / stride_h) + 1);
+ * transposed: the size conv_transpose_bind states.  y is dense in the layout of x
  * (NCHW in -> NCHW out, channels-last in -> channels-last out) and rank 3
  * when x was rank 3.  Pure host code. */
 gconv_status out_shape_and_stride(const gconv_desc *d, int32_t *rank,
@@ -366,7 +368,9 @@ gconv_status conv_backward_weight(const gconv_desc *d, const void *x, const void
  * conv_backward_weight_workspace_size exceeds it gets
  * GCONV_ERR_SCRATCH_LIMIT.  The first call with a device current looks the
  * buffer's address up on that device (make it before any stream capture
- * begins).  The call itself allocates nothing.  All calls share the buffer:
+ * begins) and keeps it for the life of the process, so the device must not
+ * be reset (cudaDeviceReset) while the library is in use.  The call itself
+ * allocates nothing.  All calls share the buffer:
  * each writes every scratch entry before reading it, so no clearing is
  * needed, but calls whose kernels overlap on the GPU race on it -- keep
  * them ordered on one stream. */

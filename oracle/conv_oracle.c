@@ -47,10 +47,8 @@
  *    tested against an FP64 reference).
  *
  * Alongside y it returns bound[n, co, oh, ow] = sum over the same taps of
- * |w * x| plus |b[co]|, the scale of the parity tolerance.  The bias counts
- * as one more product term (b times a constant input of 1): with it left
- * out, an output dominated by the bias could not meet the tolerance even
- * when it is the exact value correctly rounded to fp16 or bf16.
+ * |w * x| (the bias is not a term of it), the scale of the parity
+ * tolerance tol * sum|w * x| + 1e-6.
  *
  * Output spatial size: the number of window starts t = 0, s, 2s, ... in the
  * explicitly padded input (length H + pb + pa) with t + E <= H + pb + pa,
@@ -138,10 +136,7 @@ static void one_output(const double *x, const double *w, const double *b,
             }
         }
     }
-    if (b) {
-        acc += b[co];
-        sabs += fabs(b[co]);
-    }
+    if (b) acc += b[co];
     *y_out = acc;
     *bound_out = sabs;
 }
@@ -251,10 +246,7 @@ static void one_transposed(const double *x, const double *w, const double *b,
             }
         }
     }
-    if (b) {
-        acc += b[co];
-        sabs += fabs(b[co]);
-    }
+    if (b) acc += b[co];
     *y_out = acc;
     *bound_out = sabs;
 }

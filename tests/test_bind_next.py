@@ -255,4 +255,10 @@ def test_injected_error_on_new_entry_points():
     gc.conv_test_inject_launch_error(702)
     assert lib.conv_backward_input(ctypes.byref(fwd), FAKE, FAKE, FAKE, None) == 8
     assert gc.conv_last_cuda_error() == 702
+    # the fixed-buffer weight gradient: size check first, then the hook
+    assert need <= gc.conv_backward_weight_noalloc_limit()
+    gc.conv_test_inject_launch_error(703)
+    assert lib.conv_backward_weight_noalloc(ctypes.byref(fwd), FAKE, FAKE, FAKE, FAKE,
+                                            None) == 8
+    assert gc.conv_last_cuda_error() == 703
     gc.conv_test_inject_launch_error(0)

@@ -56,7 +56,6 @@ def im2col_conv(x, w, b, stride, pb, pa, groups):
             N, OH, OW, Cog).transpose(0, 3, 1, 2)
     if b is not None:
         y = y + b[None, :, None, None]
-        yabs = yabs + np.abs(b)[None, :, None, None]
     return y, yabs
 
 
@@ -297,7 +296,9 @@ def test_unbatched_and_rejections():
 
 def test_correct_rounding_always_passes():
     # Bias-dominated outputs: the exact value rounded to the output dtype
-    # must be inside the tolerance (|ref| <= bound and tol > half an ulp).
+    # passes, through the half-ulp term; for fp16 and bf16 some of them pass
+    # only through it (tol * sum|w*x| + 1e-6 alone is below the rounding
+    # step there), so the term is needed and is counted.
     r = rng(31)
     x = r.standard_normal((1, 64, 6, 6)) * 1e-3
     w = r.standard_normal((64, 1, 1, 1)) * 1e-2
@@ -306,11 +307,53 @@ def test_correct_rounding_always_passes():
     for name, dt in (("f32", torch.float32), ("f16", torch.float16), ("bf16", torch.bfloat16)):
         rounded = torch.from_numpy(ref).to(dt)
         assert not oracle.violations(rounded, ref, bound, name).any()
+        only = oracle.rounding_only(rounded, ref, bound, name)
+        if name != "f32":
+            assert only.any()
+        # one ulp off on those elements is outside the rule
+        if only.any():
+            got = rounded.double().numpy().copy()
+            i = tuple(np.argwhere(only)[0])
+            got[i] = ref[i] + 2.5 * oracle.half_ulp(ref[i], name)
+            assert oracle.violations(got, ref, bound, name)[i]
+
+
+def test_half_ulp_matches_the_dtype_spacing():
+    # Pinned to numpy's own float16 / float32 spacing (the gap to the next
+    # representable value) on values exactly representable in each dtype,
+    # including binade starts, fp16 subnormals and negative values.
+    r = rng(5)
+    v16 = np.concatenate([r.standard_normal(2000) * 10.0 ** r.uniform(-7, 4, 2000),
+                          [1.0, 2.0, 0.5, -4.0, 2.0 ** -14, 2.0 ** -20, 65504.0]]).astype(np.float16)
+    v16 = v16[np.isfinite(v16) & (v16 != 0) & (np.abs(v16) < 65504)]
+    np.testing.assert_array_equal(oracle.half_ulp(v16.astype(np.float64), "f16"),
+                                  np.spacing(np.abs(v16)).astype(np.float64) / 2)
+    v32 = np.concatenate([r.standard_normal(2000) * 10.0 ** r.uniform(-30, 30, 2000),
+                          [1.0, 2.0 ** -126, 2.0 ** -140, -8.0]]).astype(np.float32)
+    np.testing.assert_array_equal(oracle.half_ulp(v32.astype(np.float64), "f32"),
+                                  np.spacing(np.abs(v32)).astype(np.float64) / 2)
+    # bfloat16: spacing from the bit pattern (an 8-bit significand), via torch
+    vb = torch.from_numpy(r.standard_normal(2000) * 10.0 ** r.uniform(-20, 20, 2000)).to(
+        torch.bfloat16)
+    vb = vb[vb != 0].abs()
+    nxt = (vb.view(torch.int16) + 1).view(torch.bfloat16)
+    gap = nxt.double() - vb.double()
+    np.testing.assert_array_equal(oracle.half_ulp(vb.double().numpy(), "bf16"),
+                                  gap.numpy() / 2)
+    assert oracle.half_ulp(0.0, "bf16") == 0.0
+    # one rounding (fp32 -> dtype, as the kernels' output cast) never moves a
+    # value by more than the term, and reaches it at midpoints
+    v = r.uniform(-3, 3, 20000).astype(np.float32)
+    for name, dt in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+        moved = np.abs(torch.from_numpy(v).to(dt).double().numpy() - v.astype(np.float64))
+        ratio = moved / oracle.half_ulp(v.astype(np.float64), name)
+        assert ratio.max() <= 1.0 and ratio.max() > 0.99
 
 
 def test_tolerance_rule():
     ref = np.array([1.0, 1.0, 0.0])
-    bound = np.array([0.1, 0.1, 0.0])   # tol*bound = 2e-4 for fp16
-    got = np.array([1.0 + 1.5e-4, 1.0 + 2.5e-4, 5e-7])
+    # fp16: tol*bound = 2e-4, + 1e-6, + half an ulp of 1.0 (2^-11 = 4.88e-4)
+    bound = np.array([0.1, 0.1, 0.0])
+    got = np.array([1.0 + 6.85e-4, 1.0 + 6.95e-4, 5e-7])
     assert list(oracle.violations(got, ref, bound, "f16")) == [False, True, False]
     assert oracle.violations(np.array([np.nan]), np.array([0.0]), np.array([1.0]), "f32")[0]

@@ -63,7 +63,6 @@ def im2col_dilated(x, w, b, stride, pb, pa, groups, dil):
                 yabs[:, g * Cog:(g + 1) * Cog, i, j] = np.abs(win) @ np.abs(Wg).T
     if b is not None:
         y += b[None, :, None, None]
-        yabs += np.abs(b)[None, :, None, None]
     return y, yabs
 
 
@@ -194,7 +193,6 @@ def scatter_transposed(x, w, b, stride, pb, pa, op, groups, dil):
     yabs = fabs_[:, :, pb[0]:FH - pa[0], pb[1]:FW - pa[1]]
     if b is not None:
         y = y + b[None, :, None, None]
-        yabs = yabs + np.abs(b)[None, :, None, None]
     return y, yabs
 
 
