@@ -1,21 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of the direct-stencil convolution library on one GB300.
 
-A step is one pass of the whole path over one batch: the MobileNetV2-style
-depthwise layer (N=32, C=144, 56x56, bf16 channels-last, 3x3, padding 1/1,
-bias) at stride 1 and at stride 2, each bound, launched through the C ABI and
-written into its preallocated output.
+A step is one pass of the whole path over one batch of each benchmark
+configuration: the six convolutions of the five workloads (depthwise 3x3
+fp32 NCHW; the MobileNetV2-style bf16 channels-last depthwise layer at stride
+1 and at stride 2; the 7x7 bf16 channels-last depthwise layer; the
+multiplier-4 4x4 fp16 NCHW layer; the grouped 4->8 9x9 stride-2 bf16
+channels-last layer), each bound once, launched through the C ABI and written
+into its preallocated output.
 
 Metric: achieved HBM GB/s with algorithmic bytes = x + w + bias + y, each
-moved once, plus output pixels per second (Gpix/s = N*OH*OW / s).  Timing:
-warm-up steps, then exactly K steps replayed from CUDA graphs of back-to-back
-launches, bracketed by a barrier and a device synchronise, timed with CUDA
-events on the launching stream; max over ranks.  L2: every step reads and
-writes one of several input/output sets whose total exceeds 3x the L2 size,
-so no step finds its data in L2.
+moved once, summed over the step's convolutions, plus output pixels per
+second (Gpix/s = N*OH*OW / s).  Timing: warm-up steps, then exactly K steps
+replayed from CUDA graphs of back-to-back launches, bracketed by a barrier and
+a device synchronise, timed with CUDA events on the launching stream; max
+over ranks.  L2: every step reads and writes one of several input/output sets
+whose total exceeds 3x the L2 size, so no step finds its data in L2.  The
+MobileNetV2 pair alone is reported as a sub-entry (``mbv2_step``), every
+workload alone under ``per_config`` (with the fp64 oracle timed on the host
+cores on the same workload), and the roofline of the kernel that takes the
+largest share of the step.
 
 ``--impl reference`` times the CPU fp64 oracle (the only reference this
-method has) on a bounded sample of the same workload instead.
+method has) on a bounded sample of the same step instead.
 """
 
 from __future__ import annotations
@@ -33,11 +40,19 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-STEP_WORKLOADS = ("mbv2_dw3x3_s1_bf16_cl", "mbv2_dw3x3_s2_bf16_cl")
+# The six convolutions of the five benchmark workloads: one step.
+STEP_WORKLOADS = ("dw3x3_f32_nchw", "mbv2_dw3x3_s1_bf16_cl", "mbv2_dw3x3_s2_bf16_cl",
+                  "dw7x7_bf16_cl", "dw4x4_m4_f16_nchw", "grp4x8_9x9_s2_bf16_cl")
+# The MobileNetV2 layer at both strides, reported as its own sub-step.
+MBV2_STEP = ("mbv2_dw3x3_s1_bf16_cl", "mbv2_dw3x3_s2_bf16_cl")
+STEP_NAME = ("dw3x3 f32 NCHW 1x32x56x56 + MobileNetV2 dw3x3 bf16 CL 32x144x56x56 s1 + s2 + "
+             "dw7x7 bf16 CL 128x96x56x56 + dw4x4 m4 f16 NCHW 16x64x112x112 pad 1/2 + "
+             "grouped 4->8 9x9 s2 bf16 CL 8x256x128x128")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 # FP32 FMA lanes: 152 SMs x 128 lanes x 2070 MHz (max SM clock).
 SMS, FMA_LANES, MAX_MHZ = 152, 128, 2070.0
+DERIVED_FMA_PEAK = SMS * FMA_LANES * MAX_MHZ * 1e6
 
 
 def parse():
@@ -380,23 +395,35 @@ def time_graph(cases, steps, warmup, world, chunk=200):
 
 def time_e2e(cases, steps, world, lanes=3):
     """Same metric through the public API with host buffers: every step copies
-    its input from pinned host memory, runs the convolutions and reads the
-    results back to pinned host memory.  Steps rotate over `lanes` streams,
-    each with its own device and pinned output buffers, so step i's input
-    copy overlaps step i-1's kernels and step i-2's read-back (the copy
-    engines and the SMs work at once, as a streaming user would run them)."""
+    each distinct input from pinned host memory, runs the convolutions and
+    reads every result back to pinned host memory.  Steps rotate over `lanes`
+    streams, each with its own device and pinned output buffers, so step i's
+    input copies overlap step i-1's kernels and step i-2's read-backs (the
+    copy engines and the SMs work at once, as a streaming user would run
+    them).  Convolutions of one workload id (the MobileNetV2 layer at both
+    strides) read the same input, copied once."""
     import torch
     gc = cases[0].gc
-    host_x = cases[0].x_host.pin_memory()
     streams = [torch.cuda.Stream() for _ in range(lanes)]
-    dev_x = [cases[0].xs[0]] + [cases[0].xs[0].clone() for _ in range(lanes - 1)]
-    dev_y = [[gc.empty_output(c.desc, dev_x[0]) for c in cases] for _ in range(lanes)]
+    host_x, slot = [], []
+    for c in cases:
+        for k, (wid, _) in enumerate(host_x):
+            if wid == c.wl.wid:
+                slot.append(k)
+                break
+        else:
+            slot.append(len(host_x))
+            host_x.append((c.wl.wid, c.x_host.pin_memory()))
+    host_x = [h for _, h in host_x]
+    dev_x = [[cases[slot.index(k)].xs[0] if lane == 0 else cases[slot.index(k)].xs[0].clone()
+              for k in range(len(host_x))] for lane in range(lanes)]
+    dev_y = [[gc.empty_output(c.desc, c.xs[0]) for c in cases] for _ in range(lanes)]
     # Pinned host outputs with the device outputs' own strides (channels-last
     # stays channels-last), so each read-back is one plain copy.
     outs = [[torch.empty_strided(c.ys[0].shape, c.ys[0].stride(), dtype=c.ys[0].dtype,
                                  pin_memory=True) for c in cases]
             for _ in range(lanes)]
-    h2d = host_x.numel() * host_x.element_size()
+    h2d = sum(h.numel() * h.element_size() for h in host_x)
     d2h = sum(o.numel() * o.element_size() for o in outs[0])
     main = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -404,12 +431,13 @@ def time_e2e(cases, steps, world, lanes=3):
     def step(i):
         k = i % lanes
         with torch.cuda.stream(streams[k]):
-            dev_x[k].copy_(host_x, non_blocking=True)
-            for c, y, o in zip(cases, dev_y[k], outs[k]):
-                c.gc.run(c.desc, dev_x[k], c.w, c.b, y, streams[k])
+            for dx, hx in zip(dev_x[k], host_x):
+                dx.copy_(hx, non_blocking=True)
+            for c, s_, y, o in zip(cases, slot, dev_y[k], outs[k]):
+                c.gc.run(c.desc, dev_x[k][s_], c.w, c.b, y, streams[k])
                 o.copy_(y, non_blocking=True)
 
-    for i in range(3 * lanes):  # warm-up
+    for i in range(2 * lanes):  # warm-up
         step(i)
     torch.cuda.synchronize()
     barrier(world)
@@ -426,6 +454,46 @@ def time_e2e(cases, steps, world, lanes=3):
     return max_over_ranks(start.elapsed_time(end), world), h2d, d2h
 
 
+def measure_fma_peak(dev, reps=5):
+    """The chip's fp32 FMA rate, measured: the library's probe kernel (every
+    SM full of independent FMA chains) timed with CUDA events, best of
+    `reps` launches after one warm-up.  FMAs per second."""
+    import torch
+    import grouped_convolution_gb300 as gc
+    sink = torch.zeros(152 * 64, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    gc.conv_probe_fma_rate(64, sink, stream)
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = gc.conv_probe_fma_rate(4096, sink, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rate = n / (e0.elapsed_time(e1) * 1e-3)
+        best = rate if best is None else max(best, rate)
+    return best
+
+
+def roofline_of(c, us, hbm_peak, fma_peak):
+    """Roofline of one kernel: the bound is the resource whose peak time is
+    the larger (HBM for the algorithmic bytes, the FP32 FMA pipe for the
+    algorithmic FMAs); a tensor-core schedule is held to HBM and the bf16
+    tensor peak is not its limit at these shapes."""
+    t = us * 1e-6
+    t_hbm = c.bytes / (hbm_peak * 1e9)
+    t_fma = c.fma / fma_peak
+    if c.schedule == "grp_tc" or t_hbm >= t_fma:
+        ach = c.bytes / t / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 2), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(ach / hbm_peak, 4)}
+    ach = 2 * c.fma / t / 1e12
+    peak = 2 * fma_peak / 1e12
+    return {"bound": "alu", "achieved": round(ach, 3), "peak": round(peak, 3),
+            "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "note": "fp32 FMA pipe, 2 flops per FMA; peak = the probe's measured FMA rate"}
+
+
 def run_ours(args):
     import torch
     import grouped_convolution_gb300 as gc
@@ -438,6 +506,7 @@ def run_ours(args):
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    fma_peak = measure_fma_peak(dev)
 
     # Step cases share one rotation depth sized from their joint footprint.
     probe = [ConvCase(n, 1, dev) for n in STEP_WORKLOADS]
@@ -450,59 +519,77 @@ def run_ours(args):
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     total_ms, launches = time_graph(cases, args.steps, args.warmup, world)
+    mb_cases = [c for c in cases if c.wl.name in MBV2_STEP]
+    mb_ms, _ = time_graph(mb_cases, args.steps, args.warmup, world)
     clocks = sampler.stop()
-
-    # Per-kernel average launch time, each kernel alone over the same protocol.
-    per_kernel = {}
-    for c in cases:
-        ms, _ = time_graph([c], args.steps, args.warmup, world)
-        per_kernel[c.wl.name] = ms / args.steps
 
     step_bytes = sum(c.bytes for c in cases)
     step_pix = sum(c.pix for c in cases)
     ms_per_step = total_ms / args.steps
     value = step_bytes * args.steps * world / (total_ms * 1e-3) / 1e9
     gpix = step_pix * args.steps * world / (total_ms * 1e-3) / 1e9
+    mb_bytes = sum(c.bytes for c in mb_cases)
+    mb_value = mb_bytes * args.steps * world / (mb_ms * 1e-3) / 1e9
 
-    dom = cases[0]
-    dom_ms = per_kernel[dom.wl.name]
-    achieved = dom.bytes / (dom_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(dom.schedule, dom.wl.name)
-
-    e2e_steps = max(1, min(args.steps, 50))
+    e2e_steps = max(1, min(args.steps, 30))
     e2e_ms, h2d, d2h = time_e2e(cases, e2e_steps, world)
     e2e_value = step_bytes * e2e_steps * world / (e2e_ms * 1e-3) / 1e9
+    del cases, mb_cases
+    torch.cuda.empty_cache()
 
+    # Every workload alone (its own rotation depth): the per-kernel times
+    # behind the roofline, and the per-config record.
+    configs = per_config(args, world, l2, hbm_peak, fma_peak, dev)
+    share = {n: configs[n]["us"] for n in STEP_WORKLOADS}
+    dom_name = max(share, key=share.get)
+    dom = configs[dom_name]
+    roof = dict(dom["roofline"])
+    roof.update({"kernel": f"{dom['schedule']} ({dom_name})", "peak_kind": peak_kind,
+                 "traffic": recorded_traffic(dom["schedule"], dom_name),
+                 "algorithmic_bytes": dom["bytes"], "algorithmic_fma": dom["fma"],
+                 "launch_us": dom["us"],
+                 "share_of_kernel_time": round(share[dom_name] / sum(share.values()), 4)})
+    if roof["bound"] == "alu":
+        roof["peak_kind"] = "measured (FMA probe)"
     result = {
         "metric": "direct-stencil conv HBM GB/s (algorithmic bytes x+w+b+y once) and Gpix/s",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 in/out, fp32 accumulate", "data": "synthetic (seeded)",
-        "config": {"workload": "MobileNetV2 depthwise 3x3 bf16 channels-last N=32 C=144 "
-                               "56x56 pad 1/1 bias, stride 1 + stride 2",
-                   "convs_per_step": [c.wl.name for c in cases],
-                   "schedules": {c.wl.name: c.schedule for c in cases},
+        "dtype": "f32/bf16/f16 in/out (per workload), fp32 accumulate",
+        "data": "synthetic (seeded)",
+        "config": {"workload": STEP_NAME,
+                   "convs_per_step": list(STEP_WORKLOADS),
+                   "schedules": {n: configs[n]["schedule"] for n in STEP_WORKLOADS},
                    "l2": f"{R} rotating input/output sets, {R * per_set / 2**20:.0f} MiB "
                          f"> 3x L2 ({l2 / 2**20:.0f} MiB)",
                    "parallelism": f"replicas x{world}"},
         "gpix_per_s": round(gpix, 3),
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "frac_of_measured_hbm": round(value / world / hbm_peak, 4),
-        "per_kernel_us": {k: round(v * 1e3, 3) for k, v in per_kernel.items()},
-        "roofline": {"bound": "hbm", "kernel": f"{dom.schedule} ({dom.wl.name})",
-                     "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
-                     "traffic": traffic, "algorithmic_bytes": dom.bytes},
+        "mbv2_step": {"convs": list(MBV2_STEP), "GB_s": round(mb_value, 2),
+                      "us_per_step": round(mb_ms / args.steps * 1e3, 3),
+                      "frac_of_measured_hbm": round(mb_value / world / hbm_peak, 4)},
+        "fma_peak": {"measured_tfma_s": round(fma_peak / 1e12, 3),
+                     "derived_tfma_s": round(DERIVED_FMA_PEAK / 1e12, 3),
+                     "derived_from": "152 SMs x 128 FP32 lanes x 2070 MHz"},
+        "per_kernel_us": share,
+        "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches,
         "clocks": clocks,
     }
     if not args.no_configs:
-        result["per_config"] = per_config(args, world, l2, hbm_peak, dev)
+        result["per_config"] = configs
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        result["cpu_baseline"] = cpu_baseline(budget_s=15.0)
+        base = cpu_baseline(configs, budget_s=2.5)
+        result["cpu_baseline"] = base
+        if not args.no_configs:
+            for n, b in base.pop("per_config").items():
+                configs[n]["cpu_baseline"] = b
+        else:
+            base.pop("per_config")
     if rank == 0:
         line = json.dumps(result)
         print(line, flush=True)
@@ -514,12 +601,14 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def per_config(args, world, l2, hbm_peak, dev):
-    """Every workload alone: GB/s, Gpix/s, HBM fraction and FMA-pipe fraction."""
+def per_config(args, world, l2, hbm_peak, fma_peak, dev):
+    """Every workload alone: GB/s, Gpix/s, HBM fraction, FMA-pipe fraction
+    and the kernel's roofline.  With --no-configs only the step's workloads."""
     import torch
     from grouped_convolution_gb300.inputs import WORKLOADS
     out = {}
     steps = max(20, min(args.steps, 2000))
+
     def measure(name, schedule=None):
         one = ConvCase(name, 1, dev, schedule)
         R = sets_needed(one.footprint(), l2)
@@ -529,14 +618,15 @@ def per_config(args, world, l2, hbm_peak, dev):
         ms, _ = time_graph([c], steps, max(3, min(args.warmup, 50)), world)
         t = ms / steps * 1e-3
         gbs = c.bytes / t / 1e9
-        fma_peak = SMS * FMA_LANES * MAX_MHZ * 1e6
         res = {"schedule": c.schedule, "us": round(t * 1e6, 3),
                "GB_s": round(gbs, 1), "Gpix_s": round(c.pix / t / 1e9, 3),
                "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
                "TFMA_s": round(c.fma / t / 1e12, 3),
-               "frac_of_fma_peak_2070mhz": round(c.fma / t / fma_peak, 4),
-               "bytes": c.bytes, "fma": c.fma}
+               "frac_of_fma_peak_measured": round(c.fma / t / fma_peak, 4),
+               "frac_of_fma_peak_2070mhz": round(c.fma / t / DERIVED_FMA_PEAK, 4),
+               "roofline": roofline_of(c, t * 1e6, hbm_peak, fma_peak),
+               "bytes": c.bytes, "fma": c.fma, "rotating_sets": R}
         del c
         torch.cuda.empty_cache()
         return res
@@ -550,29 +640,31 @@ def per_config(args, world, l2, hbm_peak, dev):
         ms, _ = time_graph([c], steps, max(3, min(args.warmup, 50)), world)
         t = ms / steps * 1e-3
         gbs = c.bytes / t / 1e9
-        fma_peak = SMS * FMA_LANES * MAX_MHZ * 1e6
         res = {"pass": part, "us": round(t * 1e6, 3), "GB_s": round(gbs, 1),
                "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
                "TFMA_s": round(c.fma / t / 1e12, 3),
-               "frac_of_fma_peak_2070mhz": round(c.fma / t / fma_peak, 4),
+               "frac_of_fma_peak_measured": round(c.fma / t / fma_peak, 4),
                "bytes": c.bytes, "fma": c.fma, "launches_per_call": 1 if part == "input" else 2}
         del c
         torch.cuda.empty_cache()
         return res
 
-    for name in WORKLOADS:
+    names = list(WORKLOADS) if not args.no_configs else list(STEP_WORKLOADS)
+    for name in names:
         out[name] = measure(name)
         # A call the picker sends to the tensor cores is also timed on the
         # direct stencil (no tensor cores) that would take it otherwise.
-        if out[name]["schedule"] == "grp_tc":
+        if out[name]["schedule"] == "grp_tc" and not args.no_configs:
             st = measure(name, "grp_plane")
             out[name]["direct_stencil"] = {k: st[k] for k in (
                 "schedule", "us", "GB_s", "frac_of_measured_hbm", "TFMA_s",
-                "frac_of_fma_peak_2070mhz")}
-    # The backward of the step's layers: dx (a transposed convolution of the
-    # output gradient) and dw + db (two launches: slice partials, then the
-    # fixed-order sum).
-    for name in STEP_WORKLOADS:
+                "frac_of_fma_peak_measured", "roofline")}
+    if args.no_configs:
+        return out
+    # The backward of the MobileNetV2 layers: dx (a transposed convolution of
+    # the output gradient) and dw + db (two launches: slice partials, then
+    # the fixed-order sum).
+    for name in MBV2_STEP:
         for part in ("input", "weight"):
             out[f"{name}.backward_{part}"] = measure_bwd(name, part)
     return out
@@ -580,65 +672,105 @@ def per_config(args, world, l2, hbm_peak, dev):
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_step_sample(budget_s, max_steps=None):
-    """Time the fp64 oracle on the step's workloads, restricted to the first
-    n images, with n grown until one pass takes a measurable time."""
-    import oracle
-    from grouped_convolution_gb300.inputs import WORKLOADS, make_inputs
-    wls = [WORKLOADS[n] for n in STEP_WORKLOADS]
-    x, w, b = make_inputs(wls[0])
-    xs = x.double().contiguous()   # widening, outside the timed region
-    ws, bs = w.double(), b.double()
-    elem = x.element_size()
+class OracleSample:
+    """The fp64 oracle on one workload, restricted to its first n images
+    (inputs widened to fp64 outside the timed region)."""
 
-    def bytes_for(n_img):
-        total = 0
-        for wl in wls:
-            oh = oracle.out_size(wl.H, wl.KH, wl.stride[0], wl.pad_before[0], wl.pad_after[0])
-            ow = oracle.out_size(wl.W, wl.KW, wl.stride[1], wl.pad_before[1], wl.pad_after[1])
-            total += (n_img * wl.C_in * wl.H * wl.W + wl.C_out * wl.cin_g * wl.KH * wl.KW +
-                      wl.C_out + n_img * wl.C_out * oh * ow) * elem
-        return total
+    def __init__(self, name):
+        import oracle
+        from grouped_convolution_gb300.inputs import WORKLOADS, make_inputs
+        self.oracle = oracle
+        self.wl = wl = WORKLOADS[name]
+        x, w, b = make_inputs(wl)
+        self.elem = x.element_size()
+        self.x = x.double().contiguous()
+        self.w = w.double()
+        self.b = b.double() if b is not None else None
+        self.n_max = x.shape[0]
 
-    def one_pass(n_img):
+    def bytes_for(self, n_img):
+        wl, o = self.wl, self.oracle
+        oh = o.out_size(wl.H, wl.KH, wl.stride[0], wl.pad_before[0], wl.pad_after[0])
+        ow = o.out_size(wl.W, wl.KW, wl.stride[1], wl.pad_before[1], wl.pad_after[1])
+        return (n_img * wl.C_in * wl.H * wl.W + wl.C_out * wl.cin_g * wl.KH * wl.KW +
+                (wl.C_out if wl.bias else 0) + n_img * wl.C_out * oh * ow) * self.elem
+
+    def one_pass(self, n_img):
+        wl = self.wl
         t0 = time.perf_counter()
-        for wl in wls:
-            oracle.conv2d(xs[:n_img], ws, bs, wl.stride, wl.pad_before, wl.pad_after, wl.groups)
+        self.oracle.conv2d(self.x[:n_img], self.w, self.b, wl.stride, wl.pad_before,
+                           wl.pad_after, wl.groups)
         return time.perf_counter() - t0
 
-    return oracle, wls, one_pass, bytes_for, xs.shape[0]
+    def timed(self, budget_s):
+        """Whole passes over as many images as fit about `budget_s`: returns
+        (GB/s, images, passes, seconds)."""
+        t1 = self.one_pass(1)
+        n_img = max(1, min(self.n_max, int(budget_s / max(t1, 1e-4))))
+        self.one_pass(n_img)                    # untimed first pass at this size
+        t, reps = 0.0, 0
+        while reps < 1 or (t < budget_s and reps < 200):
+            t += self.one_pass(n_img)
+            reps += 1
+        return self.bytes_for(n_img) * reps / t / 1e9, n_img, reps, t
 
 
-def cpu_baseline(budget_s=15.0):
-    oracle, wls, one_pass, bytes_for, n_max = oracle_step_sample(budget_s)
-    n_img = n_max
-    t1 = one_pass(n_img)
-    reps = max(1, int(budget_s / max(t1, 1e-3)))
-    t = 0.0
-    for _ in range(reps):
-        t += one_pass(n_img)
-    gbs = bytes_for(n_img) * reps / t / 1e9
-    return {"value": round(gbs, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+def cpu_baseline(configs, budget_s=2.5):
+    """The oracle on every workload of the step, on the host cores: per
+    workload GB/s on a bounded sample, the step aggregate (sum of the samples'
+    bytes over the sum of their times, per image of each workload), and the
+    first workload once more on one thread."""
+    import oracle
+    per, tot_b, tot_t = {}, 0.0, 0.0
+    cores = oracle.num_threads()
+    for name in STEP_WORKLOADS:
+        smp = OracleSample(name)
+        gbs, n_img, reps, t = smp.timed(budget_s)
+        per[name] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                     "sample": f"first {n_img} of {smp.n_max} images, {reps} passes, "
+                               f"{t:.2f} s",
+                     "gpu_over_oracle": round(configs[name]["GB_s"] / gbs, 1)}
+        # whole-step aggregate: each workload's full bytes at its sampled rate
+        tot_b += smp.bytes_for(smp.n_max)
+        tot_t += smp.bytes_for(smp.n_max) / (gbs * 1e9)
+        if name == STEP_WORKLOADS[0]:
+            oracle.set_num_threads(1)
+            try:
+                g1, n1, r1, t1 = smp.timed(budget_s / 2)
+            finally:
+                oracle.set_num_threads(cores)
+            per[name]["single_thread"] = {"value": round(g1, 4), "unit": "GB/s", "cores": 1,
+                                          "sample": f"first {n1} images, {r1} passes, "
+                                                    f"{t1:.2f} s"}
+    return {"value": round(tot_b / tot_t / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"fp64 oracle, both convolutions of the step over all {n_img} images, "
-                      f"{reps} passes, {t:.1f} s"}
+            "sample": f"fp64 oracle on each of the step's {len(STEP_WORKLOADS)} convolutions "
+                      f"(about {budget_s:.1f} s of whole passes each over its first images), "
+                      "combined as the full step's bytes over its time at the sampled rates",
+            "per_config": per}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", 0))
     if rank != 0:
         return
-    oracle, wls, one_pass, bytes_for, n_max = oracle_step_sample(0)
-    t1 = one_pass(1)
+    samples = [OracleSample(n) for n in STEP_WORKLOADS]
     budget = 150.0
     per_step_budget = budget / max(1, args.steps + args.warmup)
-    n_img = max(1, min(n_max, int(per_step_budget / max(t1, 1e-4))))
+    # images per workload: the same fraction of every workload's batch
+    full = sum(s.one_pass(1) * s.n_max for s in samples)   # one step at full size, estimated
+    frac = min(1.0, per_step_budget / max(full, 1e-6))
+    n_img = [max(1, min(s.n_max, int(round(frac * s.n_max)))) for s in samples]
     for _ in range(args.warmup):
-        one_pass(n_img)
+        for s, n in zip(samples, n_img):
+            s.one_pass(n)
     t = 0.0
     for _ in range(args.steps):
-        t += one_pass(n_img)
-    gbs = bytes_for(n_img) * args.steps / t / 1e9
+        for s, n in zip(samples, n_img):
+            t += s.one_pass(n)
+    step_bytes = sum(s.bytes_for(n) for s, n in zip(samples, n_img))
+    gbs = step_bytes * args.steps / t / 1e9
+    cores = samples[0].oracle.num_threads()
     line = {
         "impl": "reference",
         "metric": "direct-stencil conv HBM GB/s (algorithmic bytes x+w+b+y once) and Gpix/s",
@@ -646,12 +778,13 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": "MobileNetV2 depthwise 3x3 bf16 channels-last N=32 C=144 "
-                               "56x56 pad 1/1 bias, stride 1 + stride 2",
-                   "sample_images_per_step": n_img},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+        "config": {"workload": STEP_NAME, "convs_per_step": list(STEP_WORKLOADS),
+                   "sample_images_per_step": dict(zip(STEP_WORKLOADS, n_img))},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
-                         "sample": f"first {n_img} of {n_max} images per step, both strides"},
+                         "sample": "first " + ", ".join(f"{n} of {s.n_max}" for s, n in
+                                                        zip(samples, n_img)) +
+                                   " images of the step's convolutions per step"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -31,7 +31,7 @@ __all__ = [
     "conv1d_bind", "conv_transpose_bind", "conv_transpose1d_bind", "conv_transpose_forward",
     "grad_input_shape_and_stride", "conv_backward_input", "conv_backward_weight_workspace_size",
     "conv_backward_weight", "conv_backward_weight_noalloc", "conv_backward_weight_noalloc_limit",
-    "conv_autotune", "conv_autotune_clear",
+    "conv_autotune", "conv_autotune_clear", "conv_probe_fma_rate",
     "conv1d", "conv_transpose2d", "conv_transpose1d",
     "conv2d_backward", "GconvError", "SCHEDULES", "lib_path",
 ]
@@ -146,6 +146,8 @@ def _load():
         lib.conv_launch_count.argtypes = []
         lib.conv_version.restype = i32
         lib.conv_version.argtypes = []
+        lib.conv_probe_fma_rate.restype = i32
+        lib.conv_probe_fma_rate.argtypes = [i32, vp, vp, P(ctypes.c_uint64)]
         _lib = lib
         return lib
 
@@ -418,6 +420,17 @@ def conv_strerror(status: int) -> str:
 
 def conv_launch_count() -> int:
     return int(_load().conv_launch_count())
+
+
+def conv_probe_fma_rate(trips: int, sink, stream=None) -> int:
+    """Launch the FMA-rate probe kernel on `stream` (`sink`: a CUDA float
+    tensor of at least SMs x resident blocks elements); returns its FMA
+    count, for the caller to divide by the time it measures."""
+    n = ctypes.c_uint64(0)
+    _check(_load().conv_probe_fma_rate(int(trips), ctypes.c_void_p(sink.data_ptr()),
+                                       _stream_ptr(stream), ctypes.byref(n)),
+           "conv_probe_fma_rate")
+    return int(n.value)
 
 
 def conv_test_inject_launch_error(cuda_error: int) -> None:

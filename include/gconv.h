@@ -407,6 +407,17 @@ int32_t conv_last_cuda_error(void);
  * threads).  Lets callers count launches inside a timed region. */
 uint64_t conv_launch_count(void);
 
+/* Measurement aid, not part of the convolution: launches one kernel of
+ * independent fp32 FMA chains sized to fill every SM (`trips` loop trips of
+ * 128 FMAs per thread) on `stream` and returns in *fmas the number of FMAs
+ * it performs, so the caller can time it with events and state the chip's
+ * FP32 FMA rate, the roofline of the FMA-bound stencils.  `sink` is a
+ * device buffer of at least (SMs x resident blocks) floats that the kernel
+ * may write (it never does for finite inputs).  Errors: GCONV_ERR_NULL,
+ * GCONV_ERR_SHAPE (trips < 1), GCONV_ERR_CUDA. */
+gconv_status conv_probe_fma_rate(int32_t trips, float *sink, gconv_stream stream,
+                                 uint64_t *fmas);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t conv_version(void);
 

@@ -82,6 +82,8 @@ def _load():
             lib.oracle_transposed_out_size.argtypes = [i64] * 7
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_set_num_threads.restype = None
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
             common = [dp, dp, dp] + [i64] * 16
             ip = ctypes.POINTER(ctypes.c_int64)
             lib.oracle_conv2d_f64.restype = ctypes.c_int
@@ -135,6 +137,11 @@ def transposed_out_size(in_size: int, k: int, s: int, pb: int, pa: int, op: int 
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's loops use from now on (results do not change)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _ptr(a: np.ndarray):

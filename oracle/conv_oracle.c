@@ -109,6 +109,16 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads for the later calls (a timing aid; the results do not depend on it). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* One output element: the sum over the group's input channels and the taps. */
 static void one_output(const double *x, const double *w, const double *b,
                        int64_t C_in, int64_t H, int64_t W,
