@@ -65,6 +65,12 @@ void note_cuda_error(int32_t e);
 // the value as the last CUDA error) instead of launching, once.
 gconv_status take_injected();
 
+// grp_tc's shift form (k_tcs.cu): stride-2 grouped calls with 4 or 8
+// channels per group whose chunk holds 8 or 16 output channels.
+bool tcs_takes(const Params &p, const void *x);
+bool tcs_supports(const gconv_desc &d, const Ptrs &q);
+cudaError_t tcs_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *launches);
+
 // Backward weight pass (k_wgrad.cu): workspace bytes, and the launches.
 uint64_t wgrad_workspace_bytes(const Params &p);
 cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *dw, void *db,

@@ -496,6 +496,7 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
 
 bool tc_supports(const gconv_desc &d, const Ptrs &q) {
     if (!plain_forward(d)) return false;                    // dilation 1, forward
+    if (tcs_supports(d, q)) return true;                    // the shift form
     if (d.layout != GCONV_LAYOUT_NHWC) return false;
     if (d.dtype != GCONV_BF16 && d.dtype != GCONV_F16) return false;   // kind::f16 operands
     if (d.KH > 9 || d.KW > 9) return false;
@@ -527,6 +528,7 @@ cudaError_t tc_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const Tc
 }
 
 cudaError_t tc_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *launches) {
+    if (tcs_takes(p, q.x)) return tcs_launch(p, q, s, launches);
     *launches = 1;
     TcGeom g;
     if (!tc_geometry(p, g)) return cudaErrorNotSupported;

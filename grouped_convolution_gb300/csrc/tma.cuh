@@ -30,6 +30,13 @@ bool tma_encode_4d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base
                    const uint64_t dims[4], const uint64_t strides_bytes[3],
                    const uint32_t box[4]);
 
+// The same with a traversal stride per dim: the box spans box[i] elements
+// of dim i and loads every element_strides[i]-th of them (box[i] /
+// element_strides[i] per dim, packed in shared memory).
+bool tma_encode_4d_strided(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                           const uint64_t dims[4], const uint64_t strides_bytes[3],
+                           const uint32_t box[4], const uint32_t element_strides[4]);
+
 // Tensor-map element type of T (float, __half or __nv_bfloat16).
 template <typename T> constexpr CUtensorMapDataType tma_dtype() {
     return sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32

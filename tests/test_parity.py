@@ -171,6 +171,14 @@ TC_CASES = [
     # blocks reused, weights restaged when a CTA's units change chunk
     ("many_units", 2, 4, 8, 64, 64, 64, 9, 9, (2, 2), (4, 4), (4, 4)),
     ("many_units_2tiles", 2, 8, 16, 32, 24, 160, 3, 3, (1, 1), (1, 1), (1, 1)),
+    # the shift form (stride 2, 8 or 16 outputs per chunk): one group per
+    # chunk, two column tiles, an even kernel with asymmetric pads, 1x1,
+    # many row bands with an odd column pad
+    ("s2_cin8", 1, 8, 8, 3, 19, 37, 5, 5, (2, 2), (2, 2), (2, 2)),
+    ("s2_wide_ct", 1, 4, 8, 2, 9, 260, 3, 3, (2, 2), (1, 1), (1, 1)),
+    ("s2_k4_asym", 2, 4, 8, 4, 14, 22, 4, 4, (2, 2), (1, 1), (2, 2)),
+    ("s2_k1", 1, 8, 8, 2, 7, 9, 1, 1, (2, 2), (0, 0), (0, 0)),
+    ("s2_tall", 1, 4, 8, 2, 70, 20, 3, 7, (2, 2), (1, 3), (1, 3)),
 ]
 
 
