@@ -215,7 +215,7 @@ KERNEL_SOURCES = {
     "dw_mult": ["k_mult.cuh", "k_mult.cu", "device_common.cuh", "tma.cuh", "launch.cuh"],
     "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh", "launch.cuh"],
     "grp_reduce": ["k_reduce.cu", "device_common.cuh", "launch.cuh"],
-    "grp_tc": ["k_tc.cu", "device_common.cuh", "tma.cuh", "launch.cuh"],
+    "grp_tc": ["k_tc.cu", "k_tcs.cu", "device_common.cuh", "tma.cuh", "tma.cu", "launch.cuh"],
     "dw_line": ["k_line.cu", "stencil_math.cuh", "device_common.cuh", "launch.cuh"],
 }
 

@@ -1,6 +1,6 @@
 // k_tcs.cu -- grp_tc's shift form: few-channel grouped convolution at
 // stride 2 (4 or 8 input channels per group, channels-last bf16/fp16) as an
-// implicit GEMM on the tcgen05 tensor cores, with the kernel columns in N.
+// implicit GEMM on the tcgen05 tensor cores, with kernel columns in N.
 //
 // The convolution is the one of torch/_inductor/kernel/conv.py
 // (LOOP_BODY_2D indexing, conv2d_template group offsets); executorch
@@ -14,30 +14,32 @@
 //    traversal stride of 2 in both spatial dims: array (ph, s) holds, for
 //    ring row i and entry e, the input pixel at row 2*(oh0 + i) - pad_h + s
 //    and column 2*(ow0 + e) - cpad + ph (cpad = pad_w rounded up to even),
-//    zero outside the image.  Each array is its rows back to back, one
-//    16-byte entry per pixel.
-//  - With tap kw + (cpad - pad_w) = 2j + ph, output column p of the tile
-//    reads entry p + j.  So A row r (the MMA's M = 128 rows) is one entry,
-//    the two K halves of an MMA (K = 16) are the ph = 0 and ph = 1 entries
-//    of one kernel row kh (s = kh & 1, ring row offset kh >> 1), and N
-//    holds the NN output channels for each of the J column shifts j:
-//      D[r][j*NN + n] = sum_{kh, ph, c} A_{kh}[r][ph, c] * w[n, c, kh, 2j + ph - dc]
+//    zero outside the image: its rows back to back, one 16-byte entry per
+//    pixel.
+//  - With tap kw + (cpad - pad_w) = 2j + ph, output column p reads entry
+//    p + j.  A row r (the MMA's M = 128 rows) is one entry; the two K
+//    halves of an MMA (K = 16) are entries r and r + 1 of one array, i.e.
+//    the shifts j = 2i and 2i + 1; N holds the NN output channels of each
+//    shift pair i (N = Jb * NN, Jb = ceil(J / 2)).  Per kernel row kh there
+//    is one MMA per phase ph (array (ph, kh & 1), ring row offset kh >> 1):
+//      D[r][i*NN + n] += sum_{h, c} A[r + h][c] * w[n, c, kh, 2(2i + h) + ph - dc]
 //    (dc = cpad - pad_w; zero weights outside the kernel or n's group).
-//    The output pixel p is the sum over j of D[p + j][j*NN + n]: each
-//    accumulator row is read once from tensor memory and the shifts are
-//    added with warp shuffles.  One MMA covers J kernel columns, so every
-//    staged entry is read by the tensor core once per kernel row instead of
-//    once per tap.
+//    Output column p is the sum over i of D[p + 2i][i*NN + n]: the Jb
+//    accumulator blocks of a row are read once from tensor memory and the
+//    shifted ones added with warp shuffles.  Each staged entry is read by
+//    the tensor core twice per kernel row instead of once per tap.
 //  - Entries of consecutive output rows follow each other in the arrays
 //    (ring row i + 1 is the next output row), so a tile is 128 consecutive
 //    entries of the band, whichever rows they belong to; tiles advance by
-//    TS = 128 - (J - 1) entries so every output finds its J shifted rows
-//    in one tile.  Row entries E = OWt + J - 1 per output row.
+//    TS = 128 - 2(Jb - 1) entries so every output finds its shifted rows
+//    in one tile.  Row entries E = OWt + 2 Jb - 1 per output row.
 //  - One CTA per SM: eight warps stage (one thread issues the TMA boxes;
 //    all stage the chunk's weights when the chunk changes) and drain tensor
-//    memory; two warps issue the MMAs of alternate tiles.  Two unit buffers
-//    and four tensor-memory tile buffers keep the tensor core fed while the
-//    next unit is staged and the previous tiles are drained.
+//    memory, the two warpgroups taking alternate tiles; four warps issue the
+//    MMAs of every fourth tile (one thread issues an MMA every ~100 cycles
+//    at best).  Two unit buffers and four tensor-memory tile buffers keep
+//    the tensor core fed while the next unit is staged and earlier tiles
+//    are drained.
 //  - Every mbarrier wait is bounded; a wait that gives up marks the CTA
 //    failed, its outputs are written as NaN, and before exiting the CTA
 //    waits (bounded) for its copies and MMAs in flight before it frees its
@@ -54,27 +56,36 @@ namespace {
 
 constexpr int kSWarps = 8;                   // staging + drain
 constexpr int kSProducers = 32 * kSWarps;
-constexpr int kSIssuers = 2;                 // MMA issue warps
-constexpr int kSThreads = kSProducers + 32 * kSIssuers;
-constexpr int kSMaxJ = 5;                    // column shifts (KW <= 9)
-constexpr int kSMaxHalf = 8;                 // output channels per drain warp
+constexpr int kSIssuers = 3;                 // MMA issue warps
+constexpr int kSLoader = kSWarps + kSIssuers;   // the warp that issues the input boxes
+constexpr int kSThreads = kSProducers + 32 * (kSIssuers + 1);
+constexpr int kSMaxJb = 3;                   // shift pairs (KW <= 9)
+constexpr int kSMaxNN = 16;                  // output channels per chunk
 constexpr int kSTileBufs = 4;
 constexpr int kSSmemCap = 220 * 1024;
 constexpr uint32_t kSSpinLimit = 1u << 22;
+// Exchange rows between the warps of a warpgroup: [warpgroup][tile parity]
+// [warp][lane < 4][(i - 1) * NN + c], lanes kSLane floats apart so the four
+// writers (and readers) of a 16-byte vector hit different banks.
+template <int NNT> constexpr int kSLane = (kSMaxJb - 1) * NNT + 4;
+constexpr int kSXchFloats = 2 * 2 * 4 * 4 * kSLane<16>;
 
 struct TcsGeom {
-    int NN, J, N;          // chunk outputs, column shifts, MMA N (16 | N)
-    int dc;                // cpad - pad_w (0 or 1)
-    int cpad;
-    int Bo, OWt, E, TS, Tn, R, Lv;
+    int NN, J, Jb, N;      // chunk outputs, column shifts, shift pairs, MMA N (16 | N)
+    int N1;                // MMA N of the ph = 1 MMAs (fewer pairs hold taps; 0: none)
+    int dc, cpad;          // cpad - pad_w (0 or 1), pad_w rounded up to even
+    int Bo, OWt, E, TS, Tn, R, R_load, Lv;
     int chunks, bands, cts, units, ctas;
     int arr_bytes;         // one (ph, s) array, 128-byte aligned
     int ring_bytes;        // the four arrays of one unit buffer
-    int b_bytes;           // one weight buffer (KH slices)
+    int b_bytes;           // one weight buffer (KH x 2 phases)
+    int raw_elems;         // the chunk's weights: NN x Cin_g x KH x KW
+    int w_dense;           // weights dense and 16-byte aligned per chunk
     int ring_off[2], b_off[2], x_off, bias_off, bar_off, smem;
     int tmem_cols;
-    uint32_t idesc;
-    FastDiv Ediv;
+    uint32_t idesc, idesc1;
+    FastDiv Ediv, Ndiv;
+    int nn_shift, cout_shift;   // log2(NN), log2(Cout_g)
     int vec_store;
 };
 
@@ -102,25 +113,32 @@ bool tcs_geometry(const Params &p, TcsGeom &g) {
     if (p.KH < 1 || p.KH > 9 || p.KW < 1 || p.KW > 9) return false;
     g.NN = (8 / p.Cin_g) * p.Cout_g;
     if (g.NN != 8 && g.NN != 16) return false;
+    g.nn_shift = g.NN == 8 ? 3 : 4;
+    g.cout_shift = 0;
+    while ((1 << g.cout_shift) < p.Cout_g) ++g.cout_shift;   // Cout_g = NN * Cin_g / 8: 4, 8 or 16
     g.dc = p.pbw & 1;
     g.cpad = p.pbw + g.dc;
     g.J = (p.KW + g.dc + 1) / 2;
-    if (g.J > kSMaxJ) return false;
-    g.N = (g.J * g.NN + 15) / 16 * 16;
-    if (g.N > 256) return false;
-    g.TS = 128 - (g.J - 1);
+    g.Jb = (g.J + 1) / 2;
+    if (g.Jb > kSMaxJb) return false;
+    g.N = (g.Jb * g.NN + 15) / 16 * 16;
+    // Phase 1 taps kw = 2j + 1 - dc: the last pair holding one may come sooner.
+    const int jmax1 = (p.KW - 2 + g.dc) / 2;   // -1 (none) when KW - 2 + dc < 0
+    g.N1 = p.KW - 2 + g.dc < 0 ? 0 : ((jmax1 / 2 + 1) * g.NN + 15) / 16 * 16;
+    g.TS = 128 - 2 * (g.Jb - 1);
     // Column tiles of at most 120 outputs; rows per unit as many (<= 8) as fit.
     g.cts = (p.OW + 119) / 120;
     g.OWt = (p.OW + g.cts - 1) / g.cts;
-    g.E = g.OWt + g.J - 1;
-    const int b_bytes = p.KH * g.N * 32;
-    g.b_bytes = (b_bytes + 127) / 128 * 128;
-    const int fixed = 2 * g.b_bytes + 2 * kSWarps * 4 * kSMaxJ * kSMaxHalf * 4 + 2 * 16 * 4 + 256;
+    g.E = g.OWt + 2 * g.Jb - 1;   // an output's last pair reads entry p + 2 Jb - 1
+    g.b_bytes = (p.KH * 2 * g.N * 32 + 127) / 128 * 128;
+    g.raw_elems = g.NN * p.Cin_g * p.KH * p.KW;
+    const int x_bytes = (g.raw_elems * 2 > kSXchFloats * 4 ? g.raw_elems * 2 : kSXchFloats * 4);
+    const int fixed = 2 * g.b_bytes + (x_bytes + 127) / 128 * 128 + 2 * 16 * 4 + 256;
     g.Bo = 0;
     for (int bo = (p.OH < 8 ? p.OH : 8); bo >= 1; --bo) {
         const int Lv = (bo - 1) * g.E + g.OWt;
         const int Tn = (Lv + g.TS - 1) / g.TS;
-        const int maxe = ((p.KH - 1) / 2) * g.E + (Tn - 1) * g.TS + 127;
+        const int maxe = ((p.KH - 1) / 2) * g.E + (Tn - 1) * g.TS + 128;
         const int R = maxe / g.E + 1;
         if (2 * R > 256 || 2 * g.E > 256) continue;   // TMA box extents
         const int arr = (R * g.E * 16 + 127) / 128 * 128;
@@ -133,6 +151,9 @@ bool tcs_geometry(const Params &p, TcsGeom &g) {
         break;
     }
     if (g.Bo == 0) return false;
+    // Rows past Bo + (KH - 1) / 2 are read only by accumulator rows that no
+    // output uses (the last tile's overrun), so they are not loaded.
+    g.R_load = g.Bo + (p.KH - 1) / 2;
     g.ring_bytes = 4 * g.arr_bytes;
     g.chunks = p.C_in / 8;
     g.bands = (p.OH + g.Bo - 1) / g.Bo;
@@ -145,7 +166,7 @@ bool tcs_geometry(const Params &p, TcsGeom &g) {
     g.b_off[0] = 2 * g.ring_bytes;
     g.b_off[1] = g.b_off[0] + g.b_bytes;
     g.x_off = g.b_off[1] + g.b_bytes;
-    g.bias_off = g.x_off + 2 * kSWarps * 4 * kSMaxJ * kSMaxHalf * 4;
+    g.bias_off = g.x_off + (x_bytes + 127) / 128 * 128;
     g.bar_off = g.bias_off + 2 * 16 * 4;
     g.smem = g.bar_off + 256;
     if (g.smem > kSSmemCap) return false;
@@ -154,7 +175,10 @@ bool tcs_geometry(const Params &p, TcsGeom &g) {
     if (pow2 > 512) return false;
     g.tmem_cols = pow2;
     g.idesc = s_idesc(p.dtype == GCONV_BF16, 128, g.N);
+    g.idesc1 = s_idesc(p.dtype == GCONV_BF16, 128, g.N1 > 0 ? g.N1 : 16);
     g.Ediv = FastDiv((uint32_t)g.E);
+    g.Ndiv = FastDiv((uint32_t)g.N);
+    g.w_dense = 0;
     g.vec_store = 0;
     return true;
 }
@@ -246,6 +270,19 @@ __device__ __forceinline__ void s_ld<8>(uint32_t taddr, float (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 template <>
+__device__ __forceinline__ void s_ld<16>(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+        "[%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <>
 __device__ __forceinline__ void s_ld<4>(uint32_t taddr, float (&v)[4]) {
     uint32_t r[4];
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
@@ -260,9 +297,12 @@ __device__ __forceinline__ void s_wait_ld() {
 __device__ __forceinline__ void s_producer_sync() {   // warps 0-7 only
     asm volatile("bar.sync 1, %0;\n" ::"n"(kSProducers) : "memory");
 }
+__device__ __forceinline__ void s_group_sync(int wg) {  // warps 4wg .. 4wg+3
+    asm volatile("bar.sync %0, 128;\n" ::"r"(2 + wg) : "memory");
+}
 
-// T: element type; HALF: output channels per drain warp (NN / 2).
-template <typename T, int HALF>
+// T: element type; NNT: output channels per chunk (8 or 16).
+template <typename T, int NNT>
 __global__ void __launch_bounds__(kSThreads, 1)
 tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
            const T *__restrict__ b, T *__restrict__ y, Params p, TcsGeom g) {
@@ -276,34 +316,37 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     const int nunits = per + ((int)blockIdx.x < extra ? 1 : 0);
     if (nunits <= 0) return;
 
-    // mbarriers: staged[2] (the unit's four boxes landed + weights and bias
-    // written: 1 expect-tx arrival + 256 producer arrivals), ring_free[2]
-    // (every MMA that read the unit buffer completed: one commit per
-    // issuer), acc_full[4] (a tile's MMAs completed), acc_empty[4] (a tile
-    // drained: 256 arrivals).
+    // mbarriers: staged[2] (a unit's four boxes landed: the loader's
+    // expect-tx arrival), ring_free[2] (every MMA that read the unit buffer
+    // completed: one commit per issuer), acc_full[4] (a tile's MMAs
+    // completed), acc_empty[4] (a tile drained by its warpgroup: 128
+    // arrivals), b_ready[2] (a chunk's weights and bias written into weight
+    // buffer i: 256 arrivals).
     const uint32_t bar_staged = sbase + (uint32_t)g.bar_off;
     const uint32_t bar_free = bar_staged + 16u;
     const uint32_t bar_full = bar_staged + 32u;
     const uint32_t bar_empty = bar_staged + 64u;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(s_smem + g.bar_off + 96);
-    volatile int *failed = reinterpret_cast<volatile int *>(s_smem + g.bar_off + 100);
+    const uint32_t bar_bready = bar_staged + 96u;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(s_smem + g.bar_off + 112);
+    volatile int *failed = reinterpret_cast<volatile int *>(s_smem + g.bar_off + 116);
     float *bias_s = reinterpret_cast<float *>(s_smem + g.bias_off);   // [2][16]
-    float *xch = reinterpret_cast<float *>(s_smem + g.x_off);        // [2][8 warps][4][J][HALF]
+    float *xch = reinterpret_cast<float *>(s_smem + g.x_off);
 
     if (warp == kSWarps) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                         sbase + (uint32_t)(g.bar_off + 96)),
+                         sbase + (uint32_t)(g.bar_off + 112)),
                      "r"(g.tmem_cols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     if (t == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_staged + 8u * i, kSProducers + 1);
+            mbar_init(bar_staged + 8u * i, 1);
             mbar_init(bar_free + 8u * i, kSIssuers);
+            mbar_init(bar_bready + 8u * i, kSProducers);
         }
         for (int i = 0; i < kSTileBufs; ++i) {
             mbar_init(bar_full + 8u * i, 1);
-            mbar_init(bar_empty + 8u * i, kSProducers);
+            mbar_init(bar_empty + 8u * i, kSProducers / 2);
         }
         *failed = 0;
         fence_barrier_init();
@@ -314,85 +357,16 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     s_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp >= kSWarps) {
-        // ---------------- MMA issue: issuer i takes tiles i, i+2, ... -------
-        const int iss = warp - kSWarps;
+    if (warp == kSLoader) {
+        // ------ input boxes: unit k into unit buffer k & 1 once the tensor
+        // core has read the unit two back ------
         if (lane == 0) {
-            const uint32_t lbo = (uint32_t)(2 * g.arr_bytes);   // ph = 1 array of the same s
-            int gt = 0;
-            for (int k = 0; k < nunits; ++k) {
+            const uint32_t box_bytes = (uint32_t)(16 * g.E * g.R_load);
+            TcsUnit u;
+            u.set(u0, g, p.N);
+            for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
                 const int ub = k & 1;
-                s_wait(bar_staged + 8u * ub, (uint32_t)((k >> 1) & 1), failed);
-                s_fence_after();
-                const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
-                const uint32_t bb = sbase + (uint32_t)g.b_off[ub];
-                for (int tt = 0; tt < g.Tn; ++tt, ++gt) {
-                    if ((gt & 1) != iss) continue;
-                    const int tb = gt & (kSTileBufs - 1);
-                    const int use = gt / kSTileBufs;
-                    if (use >= 1) s_wait(bar_empty + 8u * tb, (uint32_t)((use - 1) & 1), failed);
-                    s_fence_after();
-                    if (!*failed) {
-                        const uint32_t d = tmem + (uint32_t)(tb * g.N);
-                        for (int kh = 0; kh < p.KH; ++kh) {
-                            const int s = kh & 1, kr = kh >> 1;
-                            const uint32_t a = ring + (uint32_t)(s * g.arr_bytes) +
-                                               (uint32_t)((kr * g.E + tt * g.TS) * 16);
-                            const uint64_t ad = s_desc(a, lbo, 128);
-                            const uint64_t bd = s_desc(bb + (uint32_t)(kh * g.N * 32), 128, 256);
-                            s_mma(d, ad, bd, g.idesc, kh);
-                        }
-                    }
-                    s_commit(bar_full + 8u * tb);
-                }
-                s_commit(bar_free + 8u * ub);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ------------- staging and tensor-memory drain (warps 0-7) -------------
-        const uint32_t box_bytes = (uint32_t)(16 * g.E * g.R);
-        // Chunk c's weights into buffer ub: slice kh is an N x 16 K-major
-        // block, row n = j*NN + n' (output channel c*NN + n'), K = ph*8 + cc
-        // (chunk channel cc); zero outside the kernel and n''s group.
-        auto stage_b = [&](int c, int ub) {
-            T *bsm = reinterpret_cast<T *>(s_smem + g.b_off[ub]);
-            const int total = p.KH * g.N * 16;
-            for (int e = t; e < total; e += kSProducers) {
-                const int kk = e & 15;
-                const int n = (e >> 4) % g.N;
-                const int kh = (e >> 4) / g.N;
-                const int j = n / g.NN, np = n - j * g.NN;
-                const int ph = kk >> 3, cc = kk & 7;
-                const int kw = 2 * j + ph - g.dc;
-                const int cb = (np / p.Cout_g) * p.Cin_g;
-                float v = 0.f;
-                if (j < g.J && kw >= 0 && kw < p.KW && cc >= cb && cc < cb + p.Cin_g) {
-                    const int co = c * g.NN + np;
-                    v = load_f32(w + (int64_t)co * p.ws[0] + (int64_t)(cc - cb) * p.ws[1] +
-                                 (int64_t)kh * p.ws[2] + (int64_t)kw * p.ws[3]);
-                }
-                const int off = kh * g.N * 32 + (n >> 3) * 256 + (kk >> 3) * 128 + (n & 7) * 16 +
-                                (kk & 7) * 2;
-                *reinterpret_cast<T *>(reinterpret_cast<unsigned char *>(bsm) + off) =
-                    from_f32<T>(v);
-            }
-        };
-        int b_chunk[2] = {-1, -1};
-        // Stage unit u into buffer ub (k-th unit of this CTA): thread 0 waits
-        // until the unit two back has been read by the tensor core, then
-        // issues the four boxes; the weights are restaged when the chunk of
-        // this buffer changes (after the same wait).  Every producer then
-        // arrives on staged[ub].
-        auto stage = [&](const TcsUnit &u, int k) {
-            const int ub = k & 1;
-            const bool new_b = b_chunk[ub] != u.c;
-            // every producer has finished draining the unit that last used
-            // this buffer's bias
-            s_producer_sync();
-            if (k >= 2 && (t == 0 || new_b))
-                s_wait(bar_free + 8u * ub, (uint32_t)(((k - 2) >> 1) & 1), failed);
-            if (t == 0) {
+                if (k >= 2) s_wait(bar_free + 8u * ub, (uint32_t)(((k - 2) >> 1) & 1), failed);
                 mbar_arrive_expect_tx(bar_staged + 8u * ub, 4u * box_bytes);
                 const int oh0 = u.b * g.Bo, ow0 = u.ct * g.OWt;
                 const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
@@ -403,59 +377,218 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                                 2 * oh0 - p.pbh + s, u.n);
                 }
             }
-            if (new_b) {
-                stage_b(u.c, ub);
-                b_chunk[ub] = u.c;
+        }
+        __syncwarp();
+    } else if (warp >= kSWarps) {
+        // ------ MMA issue: issuer i takes tiles i, i+3, ... ------
+        const int iss = warp - kSWarps;
+        if (lane == 0) {
+            int gt = 0;
+            TcsUnit u;
+            u.set(u0, g, p.N);
+            int prev_c = -1, bsel = 1, bstaged = 0;   // bit i: phase of b_ready[i]
+            for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
+                const int ub = k & 1;
+                if (u.c != prev_c) {   // the weights of a new chunk, in the other buffer
+                    prev_c = u.c;
+                    bsel ^= 1;
+                    s_wait(bar_bready + 8u * bsel, (uint32_t)((bstaged >> bsel) & 1), failed);
+                    bstaged ^= 1 << bsel;
+                }
+                s_wait(bar_staged + 8u * ub, (uint32_t)((k >> 1) & 1), failed);
+                s_fence_after();
+                // Descriptors of (kh, ph)'s operands for tile 0: A from array
+                // (ph, kh & 1) at ring row kh >> 1, its second K half one
+                // entry on (leading byte offset 16); tile tt adds tt * TS
+                // entries to A's start address, the descriptor's low field
+                // in 16-byte units (no carry: shared addresses stay below
+                // 2^18).
+                const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
+                uint64_t ad0[9][2];
+#pragma unroll
+                for (int kh = 0; kh < 9; ++kh)
+#pragma unroll
+                    for (int ph = 0; ph < 2; ++ph)
+                        ad0[kh][ph] = s_desc(ring + (uint32_t)((ph * 2 + (kh & 1)) * g.arr_bytes) +
+                                                 (uint32_t)((kh >> 1) * g.E * 16),
+                                             16, 128);
+                const uint64_t bd0 = s_desc(sbase + (uint32_t)g.b_off[bsel], 128, 256);
+                const uint64_t bstep = (uint64_t)(g.N * 32 / 16);
+                for (int tt = 0; tt < g.Tn; ++tt, ++gt) {
+                    if (gt % kSIssuers != iss) continue;
+                    const int tb = gt & (kSTileBufs - 1);
+                    const int use = gt / kSTileBufs;
+                    if (use >= 1) s_wait(bar_empty + 8u * tb, (uint32_t)((use - 1) & 1), failed);
+                    s_fence_after();
+                    if (!*failed) {
+                        const uint32_t d = tmem + (uint32_t)(tb * g.N);
+                        const uint64_t toff = (uint64_t)(tt * g.TS);
+#pragma unroll
+                        for (int kh = 0; kh < 9; ++kh)
+                            if (kh < p.KH) {
+                                // (0, 0) first: it writes all N columns
+                                s_mma(d, ad0[kh][0] + toff, bd0 + (uint64_t)(2 * kh) * bstep,
+                                      g.idesc, kh);
+                                if (g.N1 > 0)
+                                    s_mma(d, ad0[kh][1] + toff,
+                                          bd0 + (uint64_t)(2 * kh + 1) * bstep, g.idesc1, 1);
+                            }
+                    }
+                    s_commit(bar_full + 8u * tb);
+                }
+                s_commit(bar_free + 8u * ub);
             }
-            if (t < g.NN)
-                bias_s[ub * 16 + t] =
-                    p.has_bias ? load_f32(b + (int64_t)(u.c * g.NN + t) * p.bs) : 0.f;
-            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-            s_arrive(bar_staged + 8u * ub);
+        }
+        __syncwarp();
+    } else {
+        // ------------- staging and tensor-memory drain (warps 0-7) -------------
+        // Chunk c's weights into weight buffer bsel.  First the chunk's raw
+        // weights [NN][Cin_g][KH][KW] into shared memory (16-byte loads when
+        // they are dense and aligned), then the operand: block (kh, ph) is an
+        // N x 16 K-major matrix whose row n = i*NN + n' (output channel
+        // c*NN + n') holds at K = h*8 + cc the weight of chunk channel cc at
+        // kernel column 2(2i + h) + ph - dc, zero outside the kernel and
+        // outside n''s group.  The raw copy shares the exchange buffer
+        // (every producer is inside stage() here).
+        auto stage_b = [&](int c, int bsel) {
+            T *raw = reinterpret_cast<T *>(xch);
+            if (g.w_dense) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(w + (int64_t)c * g.raw_elems);
+                for (int v = t; v < g.raw_elems / 8; v += kSProducers)
+                    reinterpret_cast<uint4 *>(raw)[v] = __ldg(src + v);
+            } else {
+                const int khw = p.KH * p.KW;
+                for (int e = t; e < g.raw_elems; e += kSProducers) {
+                    const int np = e / (p.Cin_g * khw);
+                    const int r1 = e - np * p.Cin_g * khw;
+                    const int ci = r1 / khw, r2 = r1 - ci * khw;
+                    const int kh = r2 / p.KW, kw = r2 - kh * p.KW;
+                    raw[e] = w[(int64_t)(c * g.NN + np) * p.ws[0] + (int64_t)ci * p.ws[1] +
+                               (int64_t)kh * p.ws[2] + (int64_t)kw * p.ws[3]];
+                }
+            }
+            s_producer_sync();
+            unsigned char *bsm = s_smem + g.b_off[bsel];
+            const int rows = p.KH * 2 * g.N;
+            for (int row = t; row < rows; row += kSProducers) {
+                const int kp = (int)g.Ndiv.div((uint32_t)row);   // 2 kh + ph
+                const int kh = kp >> 1, ph = kp & 1;
+                const int n = row - kp * g.N;
+                const int i = n >> g.nn_shift, np = n & (g.NN - 1);
+                const int cb = (np >> g.cout_shift) * p.Cin_g;
+                unsigned char *dst = bsm + kp * g.N * 32 + (n >> 3) * 256 + (n & 7) * 16;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = 2 * i + h;
+                    const int kw = 2 * j + ph - g.dc;
+                    const bool kw_ok = i < g.Jb && j < g.J && kw >= 0 && kw < p.KW;
+                    float v[8];
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const bool ok = kw_ok && cc >= cb && cc < cb + p.Cin_g;
+                        const int ri = ok ? ((np * p.Cin_g + cc - cb) * p.KH + kh) * p.KW + kw : 0;
+                        const float f = Elem<T>::to_f32(raw[ri]);
+                        v[cc] = ok ? f : 0.f;
+                    }
+                    uint4 o;
+                    o.x = pack2(v[0], v[1], (T *)nullptr);
+                    o.y = pack2(v[2], v[3], (T *)nullptr);
+                    o.z = pack2(v[4], v[5], (T *)nullptr);
+                    o.w = pack2(v[6], v[7], (T *)nullptr);
+                    *reinterpret_cast<uint4 *>(dst + h * 128) = o;
+                }
+            }
+        };
+        int prev_c = -1, bsel = 1;
+        int ubsel_bits = 0;   // bit ub: the weight buffer of the unit in unit buffer ub
+        // Before unit u (the k-th of this CTA): when its chunk differs from
+        // the previous unit's, its weights and bias go to the other weight
+        // buffer once the units that read that buffer (at least two back)
+        // are through the tensor core; then every producer arrives on
+        // b_ready of that buffer.
+        auto stage = [&](const TcsUnit &u, int k) {
+            const int ub = k & 1;
+            if (u.c != prev_c) {
+                prev_c = u.c;
+                bsel ^= 1;
+                // every producer is done with the exchange buffer (the raw
+                // weights go there) and with the bias of two chunks back
+                s_producer_sync();
+                if (k >= 2) s_wait(bar_free + 8u * ub, (uint32_t)(((k - 2) >> 1) & 1), failed);
+                stage_b(u.c, bsel);
+                if (t < g.NN)
+                    bias_s[bsel * 16 + t] =
+                        p.has_bias ? load_f32(b + (int64_t)(u.c * g.NN + t) * p.bs) : 0.f;
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                s_producer_sync();   // the raw copy in the exchange buffer is done with
+                s_arrive(bar_bready + 8u * bsel);
+            }
+            ubsel_bits = (ubsel_bits & ~(1 << ub)) | (bsel << ub);
         };
 
-        // Drain tile tt of unit u (global tile gt): warp (qd, hf) reads its
-        // 32 accumulator rows' HALF columns of every shift j, adds the
-        // shifted rows (shuffles inside the warp, the next warp's first
-        // rows through shared memory), the bias, rounds once, stores.
-        const int qd = warp & 3, hf = warp >> 2;
+        // Drain tile tt of unit u (global tile gt): warpgroup gt & 1 takes
+        // it (the two warpgroups drain alternate tiles).  Warp qd reads its
+        // 32 accumulator rows, all NN columns of every shift pair i, adds
+        // the rows 2i below (shuffles inside the warp, the next warp's first
+        // rows through shared memory), the bias, rounds once and stores 2 * NN
+        // bytes per output pixel.
+        const int qd = warp & 3, wg = warp >> 2;
         auto drain = [&](const TcsUnit &u, int k, int tt, int gt) {
             const int ub = k & 1;
             const int tb = gt & (kSTileBufs - 1);
             s_wait(bar_full + 8u * tb, (uint32_t)((gt / kSTileBufs) & 1), failed);
             s_fence_after();
-            float a[kSMaxJ][HALF];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) +
-                                   (uint32_t)(tb * g.N + hf * HALF);
+            float a[kSMaxJb][NNT];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(tb * g.N);
 #pragma unroll
-            for (int j = 0; j < kSMaxJ; ++j)
-                if (j < g.J) s_ld<HALF>(taddr + (uint32_t)(j * g.NN), a[j]);
+            for (int i = 0; i < kSMaxJb; ++i)
+                if (i < g.Jb) s_ld<NNT>(taddr + (uint32_t)(i * NNT), a[i]);
             s_wait_ld();
             s_fence_before();
             s_arrive(bar_empty + 8u * tb);
-            // rows 0 .. J-2 of this warp, for the warp holding the rows below
-            float *xw = xch + ((gt & 1) * kSWarps + warp) * (4 * kSMaxJ * kSMaxHalf);
-            if (lane < g.J - 1) {
+            // Row m < 2 (Jb - 1) of this warp is read at pair i (2i > m) by
+            // row m - 2i + 32 of the warp above: lane m stores those pairs.
+            constexpr int kLane = kSLane<NNT>;
+            constexpr int kXW = 4 * kLane;   // floats per warp
+            float *xw = xch + ((wg * 2 + ((gt >> 1) & 1)) * 4 + qd) * kXW;
+            if (lane < 2 * (g.Jb - 1)) {
 #pragma unroll
-                for (int j = 1; j < kSMaxJ; ++j)
+                for (int i = 1; i < kSMaxJb; ++i)
+                    if (i < g.Jb && 2 * i > lane) {
 #pragma unroll
-                    for (int c = 0; c < HALF; ++c)
-                        if (j < g.J) xw[(lane * kSMaxJ + j) * kSMaxHalf + c] = a[j][c];
+                        for (int c4 = 0; c4 < NNT / 4; ++c4)
+                            *reinterpret_cast<float4 *>(xw + lane * kLane + (i - 1) * NNT + 4 * c4) =
+                                make_float4(a[i][4 * c4], a[i][4 * c4 + 1], a[i][4 * c4 + 2],
+                                            a[i][4 * c4 + 3]);
+                    }
             }
-            s_producer_sync();
-            const float *xn = xch + ((gt & 1) * kSWarps + (warp + 1)) * (4 * kSMaxJ * kSMaxHalf);
-            float acc[HALF];
+            s_group_sync(wg);
+            const float *xn = xw + kXW;   // the next warp of the group (qd + 1)
+            float acc[NNT];
 #pragma unroll
-            for (int c = 0; c < HALF; ++c) acc[c] = a[0][c];
+            for (int c = 0; c < NNT; ++c) acc[c] = a[0][c];
 #pragma unroll
-            for (int j = 1; j < kSMaxJ; ++j) {
-                if (j >= g.J) break;
+            for (int i = 1; i < kSMaxJb; ++i) {
+                if (i >= g.Jb) break;
+                float sh[NNT];
 #pragma unroll
-                for (int c = 0; c < HALF; ++c) {
-                    float v = __shfl_down_sync(0xffffffffu, a[j][c], j);
-                    if (lane + j >= 32) v = qd < 3 ? xn[((lane + j - 32) * kSMaxJ + j) * kSMaxHalf + c] : 0.f;
-                    acc[c] += v;
+                for (int c = 0; c < NNT; ++c) sh[c] = __shfl_down_sync(0xffffffffu, a[i][c], 2 * i);
+                if (lane + 2 * i >= 32) {   // the row lies in the next warp (or past the tile)
+                    const int m = lane + 2 * i - 32;
+#pragma unroll
+                    for (int c4 = 0; c4 < NNT / 4; ++c4) {
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (qd < 3)
+                            v = *reinterpret_cast<const float4 *>(xn + m * kLane + (i - 1) * NNT +
+                                                                  4 * c4);
+                        sh[4 * c4] = v.x;
+                        sh[4 * c4 + 1] = v.y;
+                        sh[4 * c4 + 2] = v.z;
+                        sh[4 * c4 + 3] = v.w;
+                    }
                 }
+#pragma unroll
+                for (int c = 0; c < NNT; ++c) acc[c] += sh[c];
             }
             const int r = 32 * qd + lane;
             const int vpos = tt * g.TS + r;
@@ -466,30 +599,26 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                             ow < p.OW;
             if (!ok) return;
             const bool bad = *failed != 0;
-            float f[HALF];
+            const float *bs = bias_s + ((ubsel_bits >> ub) & 1) * 16;
+            float f[NNT];
 #pragma unroll
-            for (int c = 0; c < HALF; ++c)
-                f[c] = bad ? __int_as_float(0x7fc00000) : acc[c] + bias_s[ub * 16 + hf * HALF + c];
-            const int co0 = u.c * g.NN + hf * HALF;
+            for (int c = 0; c < NNT; ++c) f[c] = bad ? __int_as_float(0x7fc00000) : acc[c] + bs[c];
+            const int co0 = u.c * NNT;
             T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)oh * p.ys[2] + (int64_t)ow * p.ys[3] +
                     (int64_t)co0 * p.ys[1];
             if (g.vec_store) {
-                if constexpr (HALF == 8) {
+#pragma unroll
+                for (int v8 = 0; v8 < NNT / 8; ++v8) {
                     uint4 o;
-                    o.x = pack2(f[0], f[1], (T *)nullptr);
-                    o.y = pack2(f[2], f[3], (T *)nullptr);
-                    o.z = pack2(f[4], f[5], (T *)nullptr);
-                    o.w = pack2(f[6], f[7], (T *)nullptr);
-                    *reinterpret_cast<uint4 *>(yp) = o;
-                } else {
-                    uint2 o;
-                    o.x = pack2(f[0], f[1], (T *)nullptr);
-                    o.y = pack2(f[2], f[3], (T *)nullptr);
-                    *reinterpret_cast<uint2 *>(yp) = o;
+                    o.x = pack2(f[8 * v8 + 0], f[8 * v8 + 1], (T *)nullptr);
+                    o.y = pack2(f[8 * v8 + 2], f[8 * v8 + 3], (T *)nullptr);
+                    o.z = pack2(f[8 * v8 + 4], f[8 * v8 + 5], (T *)nullptr);
+                    o.w = pack2(f[8 * v8 + 6], f[8 * v8 + 7], (T *)nullptr);
+                    reinterpret_cast<uint4 *>(yp)[v8] = o;
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < HALF; ++c) yp[(int64_t)c * p.ys[1]] = from_f32<T>(f[c]);
+                for (int c = 0; c < NNT; ++c) yp[(int64_t)c * p.ys[1]] = from_f32<T>(f[c]);
             }
         };
 
@@ -501,19 +630,18 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         int gt = 0;
         for (int k = 0; k < nunits; ++k) {
             if (k + 1 < nunits) stage(nxt, k + 1);
-            for (int tt = 0; tt < g.Tn; ++tt, ++gt) drain(cur, k, tt, gt);
+            for (int tt = 0; tt < g.Tn; ++tt, ++gt)
+                if ((gt & 1) == wg) drain(cur, k, tt, gt);
             cur = nxt;
             nxt.next(g, p.N);
         }
     }
-    // Clean-up: after a failed wait, wait (bounded) for the last unit's
-    // boxes and MMAs before the shared and tensor memory go away.
+    // Clean-up: the last unit's commits (and, after a failed wait, its
+    // boxes) land before the shared and tensor memory go away.
     s_fence_before();
     __syncthreads();
     s_fence_after();
     if (t == 0) {
-        // the last unit's commits (and, after a failure, its boxes) have
-        // landed before the barriers' memory is released
         const int kl = nunits - 1;
         if (*failed)
             for (int k = kl > 0 ? kl - 1 : 0; k <= kl; ++k)
@@ -534,23 +662,23 @@ cudaError_t tcs_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const T
     const uint64_t dims[4] = {(uint64_t)p.C_in, (uint64_t)p.W, (uint64_t)p.H, (uint64_t)p.N};
     const uint64_t strides[3] = {(uint64_t)p.xs[3] * sizeof(T), (uint64_t)p.xs[2] * sizeof(T),
                                  (uint64_t)p.xs[0] * sizeof(T)};
-    const uint32_t box[4] = {8u, (uint32_t)(2 * g.E), (uint32_t)(2 * g.R), 1u};
+    const uint32_t box[4] = {8u, (uint32_t)(2 * g.E), (uint32_t)(2 * g.R_load), 1u};
     const uint32_t estr[4] = {1u, 2u, 2u, 1u};
     if (!tma_encode_4d_strided(&map, tma_dtype<T>(), q.x, dims, strides, box, estr))
         return cudaErrorInvalidValue;
     cudaError_t e;
     if (g.NN == 16) {
+        e = cudaFuncSetAttribute(tcs_kernel<T, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g.smem);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(tcs_kernel<T, 16>, dim3(g.ctas), dim3(kSThreads), g.smem, s, map,
+                       static_cast<const T *>(q.w), static_cast<const T *>(q.b),
+                       static_cast<T *>(q.y), p, g);
+    } else {
         e = cudaFuncSetAttribute(tcs_kernel<T, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  g.smem);
         if (e != cudaSuccess) return e;
         e = launch_pdl(tcs_kernel<T, 8>, dim3(g.ctas), dim3(kSThreads), g.smem, s, map,
-                       static_cast<const T *>(q.w), static_cast<const T *>(q.b),
-                       static_cast<T *>(q.y), p, g);
-    } else {
-        e = cudaFuncSetAttribute(tcs_kernel<T, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 g.smem);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(tcs_kernel<T, 4>, dim3(g.ctas), dim3(kSThreads), g.smem, s, map,
                        static_cast<const T *>(q.w), static_cast<const T *>(q.b),
                        static_cast<T *>(q.y), p, g);
     }
@@ -578,9 +706,13 @@ cudaError_t tcs_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *laun
     *launches = 1;
     TcsGeom g;
     if (!tcs_geometry(p, g)) return cudaErrorNotSupported;
-    const int half = g.NN / 2;
-    g.vec_store = aligned(q.y, 2 * half) && p.ys[1] == 1 && p.ys[3] % half == 0 &&
-                  p.ys[2] % half == 0 && p.ys[0] % half == 0;
+    // the chunk's weights as one dense run of 16-byte vectors
+    g.w_dense = p.ws[3] == 1 && p.ws[2] == p.KW && p.ws[1] == (int64_t)p.KH * p.KW &&
+                p.ws[0] == (int64_t)p.Cin_g * p.KH * p.KW && g.raw_elems % 8 == 0 &&
+                aligned(q.w, 16);
+    // 16-byte stores of 8 output channels
+    g.vec_store = aligned(q.y, 16) && p.ys[1] == 1 && p.ys[3] % 8 == 0 && p.ys[2] % 8 == 0 &&
+                  p.ys[0] % 8 == 0;
     if (p.dtype == GCONV_BF16) return tcs_launch_t<__nv_bfloat16>(p, q, s, g);
     return tcs_launch_t<__half>(p, q, s, g);
 }
