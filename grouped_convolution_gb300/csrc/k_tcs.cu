@@ -37,7 +37,7 @@
 //    all stage the chunk's weights when the chunk changes) and drain tensor
 //    memory, the two warpgroups taking alternate tiles; four warps issue the
 //    MMAs of every fourth tile (one thread issues an MMA every ~100 cycles
-//    at best).  Two unit buffers and four tensor-memory tile buffers keep
+//    at best).  Two unit buffers and eight tensor-memory tile buffers keep
 //    the tensor core fed while the next unit is staged and earlier tiles
 //    are drained.
 //  - Every mbarrier wait is bounded; a wait that gives up marks the CTA
@@ -61,7 +61,7 @@ constexpr int kSLoader = kSWarps + kSIssuers;   // the warp that issues the inpu
 constexpr int kSThreads = kSProducers + 32 * (kSIssuers + 1);
 constexpr int kSMaxJb = 3;                   // shift pairs (KW <= 9)
 constexpr int kSMaxNN = 16;                  // output channels per chunk
-constexpr int kSTileBufs = 4;
+constexpr int kSTileBufs = 8;                // tensor-memory tile buffers (N <= 48: 384 columns)
 constexpr int kSSmemCap = 220 * 1024;
 constexpr uint32_t kSSpinLimit = 1u << 22;
 // Exchange rows between the warps of a warpgroup: [warpgroup][tile parity]
@@ -168,7 +168,7 @@ bool tcs_geometry(const Params &p, TcsGeom &g) {
     g.x_off = g.b_off[1] + g.b_bytes;
     g.bias_off = g.x_off + (x_bytes + 127) / 128 * 128;
     g.bar_off = g.bias_off + 2 * 16 * 4;
-    g.smem = g.bar_off + 256;
+    g.smem = g.bar_off + 32 + 16 * kSTileBufs + 32;
     if (g.smem > kSSmemCap) return false;
     int cols = kSTileBufs * g.N, pow2 = 32;
     while (pow2 < cols) pow2 *= 2;
@@ -325,16 +325,17 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     const uint32_t bar_staged = sbase + (uint32_t)g.bar_off;
     const uint32_t bar_free = bar_staged + 16u;
     const uint32_t bar_full = bar_staged + 32u;
-    const uint32_t bar_empty = bar_staged + 64u;
-    const uint32_t bar_bready = bar_staged + 96u;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(s_smem + g.bar_off + 112);
-    volatile int *failed = reinterpret_cast<volatile int *>(s_smem + g.bar_off + 116);
+    const uint32_t bar_empty = bar_full + 8u * kSTileBufs;
+    const uint32_t bar_bready = bar_empty + 8u * kSTileBufs;
+    constexpr int kSlot = 32 + 16 * kSTileBufs + 16;   // byte offset of the TMEM address slot
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(s_smem + g.bar_off + kSlot);
+    volatile int *failed = reinterpret_cast<volatile int *>(s_smem + g.bar_off + kSlot + 4);
     float *bias_s = reinterpret_cast<float *>(s_smem + g.bias_off);   // [2][16]
     float *xch = reinterpret_cast<float *>(s_smem + g.x_off);
 
     if (warp == kSWarps) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                         sbase + (uint32_t)(g.bar_off + 112)),
+                         sbase + (uint32_t)(g.bar_off + kSlot)),
                      "r"(g.tmem_cols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
@@ -416,7 +417,7 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                 const uint64_t bstep = (uint64_t)(g.N * 32 / 16);
                 for (int tt = 0; tt < g.Tn; ++tt, ++gt) {
                     if (gt % kSIssuers != iss) continue;
-                    const int tb = gt & (kSTileBufs - 1);
+                    const int tb = gt % kSTileBufs;
                     const int use = gt / kSTileBufs;
                     if (use >= 1) s_wait(bar_empty + 8u * tb, (uint32_t)((use - 1) & 1), failed);
                     s_fence_after();
@@ -453,9 +454,21 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         auto stage_b = [&](int c, int bsel) {
             T *raw = reinterpret_cast<T *>(xch);
             if (g.w_dense) {
+                // at most 16 x 8 x 81 / 8 = 1296 vectors: six per thread, all
+                // loads in flight before the stores
                 const uint4 *src = reinterpret_cast<const uint4 *>(w + (int64_t)c * g.raw_elems);
-                for (int v = t; v < g.raw_elems / 8; v += kSProducers)
-                    reinterpret_cast<uint4 *>(raw)[v] = __ldg(src + v);
+                constexpr int kV = 6;
+                uint4 v[kV];
+#pragma unroll
+                for (int i = 0; i < kV; ++i) {
+                    const int e = t + i * kSProducers;
+                    v[i] = e < g.raw_elems / 8 ? __ldg(src + e) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < kV; ++i) {
+                    const int e = t + i * kSProducers;
+                    if (e < g.raw_elems / 8) reinterpret_cast<uint4 *>(raw)[e] = v[i];
+                }
             } else {
                 const int khw = p.KH * p.KW;
                 for (int e = t; e < g.raw_elems; e += kSProducers) {
@@ -535,7 +548,7 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         const int qd = warp & 3, wg = warp >> 2;
         auto drain = [&](const TcsUnit &u, int k, int tt, int gt) {
             const int ub = k & 1;
-            const int tb = gt & (kSTileBufs - 1);
+            const int tb = gt % kSTileBufs;
             s_wait(bar_full + 8u * tb, (uint32_t)((gt / kSTileBufs) & 1), failed);
             s_fence_after();
             float a[kSMaxJb][NNT];
