@@ -236,6 +236,24 @@ __device__ __forceinline__ void s_wait_final(uint32_t bar, uint32_t parity) {
         if (done) return;
     }
 }
+// The same wait by a whole warp: every lane polls and the warp leaves the
+// loop together, so the code after it stays warp-uniform.
+__device__ __forceinline__ bool s_wait_warp(uint32_t bar, uint32_t parity, volatile int *failed) {
+    for (uint32_t i = 0; i < kSSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (__all_sync(0xffffffffu, done != 0)) return true;
+        if (__any_sync(0xffffffffu, *failed != 0)) return false;
+    }
+    *failed = 1;
+    return false;
+}
 __device__ __forceinline__ void s_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
@@ -245,16 +263,37 @@ __device__ __forceinline__ void s_fence_before() {
 __device__ __forceinline__ void s_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
-__device__ __forceinline__ void s_mma(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
-                                      uint32_t idesc, int accumulate) {
+// Issue forms for a converged warp: lane 0 issues, the other lanes pass
+// over the predicated instruction, so the warp never diverges around the
+// issue and its operands stay warp-uniform.
+__device__ __forceinline__ void s_mma_lane0(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, int accumulate, uint32_t lane) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 e, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(lane));
 }
-__device__ __forceinline__ void s_commit(uint32_t bar) {
+__device__ __forceinline__ void s_commit_lane0(uint32_t bar, uint32_t lane) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+        "{\n\t.reg .pred e;\n\tsetp.eq.u32 e, %1, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(bar),
+        "r"(lane)
+        : "memory");
+}
+__device__ __forceinline__ void s_expect_tx_lane0(uint32_t bar, uint32_t bytes, uint32_t lane) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\tsetp.eq.u32 e, %2, 0;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}\n" ::"r"(bar),
+        "r"(bytes), "r"(lane)
+        : "memory");
+}
+__device__ __forceinline__ void s_tma_lane0(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0,
+                                            int c1, int c2, int c3, uint32_t lane) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\tsetp.eq.u32 e, %7, 0;\n\t"
+        "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(lane)
         : "memory");
 }
 template <int NC>
@@ -361,86 +400,83 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     if (warp == kSLoader) {
         // ------ input boxes: unit k into unit buffer k & 1 once the tensor
         // core has read the unit two back ------
-        if (lane == 0) {
-            const uint32_t box_bytes = (uint32_t)(16 * g.E * g.R_load);
-            TcsUnit u;
-            u.set(u0, g, p.N);
-            for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
-                const int ub = k & 1;
-                if (k >= 2) s_wait(bar_free + 8u * ub, (uint32_t)(((k - 2) >> 1) & 1), failed);
-                mbar_arrive_expect_tx(bar_staged + 8u * ub, 4u * box_bytes);
-                const int oh0 = u.b * g.Bo, ow0 = u.ct * g.OWt;
-                const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
-                for (int a = 0; a < 4; ++a) {
-                    const int ph = a >> 1, s = a & 1;
-                    tma_load_4d(ring + (uint32_t)((ph * 2 + s) * g.arr_bytes), &xmap,
-                                bar_staged + 8u * ub, 8 * u.c, 2 * ow0 - g.cpad + ph,
-                                2 * oh0 - p.pbh + s, u.n);
-                }
+        // The whole warp runs the loop; lane 0 issues.
+        const uint32_t box_bytes = (uint32_t)(16 * g.E * g.R_load);
+        TcsUnit u;
+        u.set(u0, g, p.N);
+        for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
+            const int ub = k & 1;
+            if (k >= 2) s_wait_warp(bar_free + 8u * ub, (uint32_t)(((k - 2) >> 1) & 1), failed);
+            s_expect_tx_lane0(bar_staged + 8u * ub, 4u * box_bytes, (uint32_t)lane);
+            const int oh0 = u.b * g.Bo, ow0 = u.ct * g.OWt;
+            const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int ph = a >> 1, s = a & 1;
+                s_tma_lane0(ring + (uint32_t)((ph * 2 + s) * g.arr_bytes), &xmap,
+                            bar_staged + 8u * ub, 8 * u.c, 2 * ow0 - g.cpad + ph,
+                            2 * oh0 - p.pbh + s, u.n, (uint32_t)lane);
             }
         }
-        __syncwarp();
     } else if (warp >= kSWarps) {
-        // ------ MMA issue: issuer i takes tiles i, i+3, ... ------
+        // ------ MMA issue: issuer i takes tiles i, i+3, ...; the whole warp
+        // runs the loop (warp-uniform descriptors), lane 0 issues ------
         const int iss = warp - kSWarps;
-        if (lane == 0) {
-            int gt = 0;
-            TcsUnit u;
-            u.set(u0, g, p.N);
-            int prev_c = -1, bsel = 1, bstaged = 0;   // bit i: phase of b_ready[i]
-            for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
-                const int ub = k & 1;
-                if (u.c != prev_c) {   // the weights of a new chunk, in the other buffer
-                    prev_c = u.c;
-                    bsel ^= 1;
-                    s_wait(bar_bready + 8u * bsel, (uint32_t)((bstaged >> bsel) & 1), failed);
-                    bstaged ^= 1 << bsel;
-                }
-                s_wait(bar_staged + 8u * ub, (uint32_t)((k >> 1) & 1), failed);
-                s_fence_after();
-                // Descriptors of (kh, ph)'s operands for tile 0: A from array
-                // (ph, kh & 1) at ring row kh >> 1, its second K half one
-                // entry on (leading byte offset 16); tile tt adds tt * TS
-                // entries to A's start address, the descriptor's low field
-                // in 16-byte units (no carry: shared addresses stay below
-                // 2^18).
-                const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
-                uint64_t ad0[9][2];
-#pragma unroll
-                for (int kh = 0; kh < 9; ++kh)
-#pragma unroll
-                    for (int ph = 0; ph < 2; ++ph)
-                        ad0[kh][ph] = s_desc(ring + (uint32_t)((ph * 2 + (kh & 1)) * g.arr_bytes) +
-                                                 (uint32_t)((kh >> 1) * g.E * 16),
-                                             16, 128);
-                const uint64_t bd0 = s_desc(sbase + (uint32_t)g.b_off[bsel], 128, 256);
-                const uint64_t bstep = (uint64_t)(g.N * 32 / 16);
-                for (int tt = 0; tt < g.Tn; ++tt, ++gt) {
-                    if (gt % kSIssuers != iss) continue;
-                    const int tb = gt % kSTileBufs;
-                    const int use = gt / kSTileBufs;
-                    if (use >= 1) s_wait(bar_empty + 8u * tb, (uint32_t)((use - 1) & 1), failed);
-                    s_fence_after();
-                    if (!*failed) {
-                        const uint32_t d = tmem + (uint32_t)(tb * g.N);
-                        const uint64_t toff = (uint64_t)(tt * g.TS);
-#pragma unroll
-                        for (int kh = 0; kh < 9; ++kh)
-                            if (kh < p.KH) {
-                                // (0, 0) first: it writes all N columns
-                                s_mma(d, ad0[kh][0] + toff, bd0 + (uint64_t)(2 * kh) * bstep,
-                                      g.idesc, kh);
-                                if (g.N1 > 0)
-                                    s_mma(d, ad0[kh][1] + toff,
-                                          bd0 + (uint64_t)(2 * kh + 1) * bstep, g.idesc1, 1);
-                            }
-                    }
-                    s_commit(bar_full + 8u * tb);
-                }
-                s_commit(bar_free + 8u * ub);
+        int gt = 0;
+        TcsUnit u;
+        u.set(u0, g, p.N);
+        int prev_c = -1, bsel = 1, bstaged = 0;   // bit i: phase of b_ready[i]
+        for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
+            const int ub = k & 1;
+            if (u.c != prev_c) {   // the weights of a new chunk, in the other buffer
+                prev_c = u.c;
+                bsel ^= 1;
+                s_wait_warp(bar_bready + 8u * bsel, (uint32_t)((bstaged >> bsel) & 1), failed);
+                bstaged ^= 1 << bsel;
             }
+            s_wait_warp(bar_staged + 8u * ub, (uint32_t)((k >> 1) & 1), failed);
+            s_fence_after();
+            // Descriptors of (kh, ph)'s operands for tile 0: A from array
+            // (ph, kh & 1) at ring row kh >> 1, its second K half one entry
+            // on (leading byte offset 16); tile tt adds tt * TS entries to
+            // A's start address, the descriptor's low field in 16-byte units
+            // (no carry: shared addresses stay below 2^18).
+            const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
+            uint64_t ad0[9][2];
+#pragma unroll
+            for (int kh = 0; kh < 9; ++kh)
+#pragma unroll
+                for (int ph = 0; ph < 2; ++ph)
+                    ad0[kh][ph] = s_desc(ring + (uint32_t)((ph * 2 + (kh & 1)) * g.arr_bytes) +
+                                             (uint32_t)((kh >> 1) * g.E * 16),
+                                         16, 128);
+            const uint64_t bd0 = s_desc(sbase + (uint32_t)g.b_off[bsel], 128, 256);
+            const uint64_t bstep = (uint64_t)(g.N * 32 / 16);
+            for (int tt = 0; tt < g.Tn; ++tt, ++gt) {
+                if (gt % kSIssuers != iss) continue;
+                const int tb = gt % kSTileBufs;
+                const int use = gt / kSTileBufs;
+                if (use >= 1) s_wait_warp(bar_empty + 8u * tb, (uint32_t)((use - 1) & 1), failed);
+                s_fence_after();
+                if (!__any_sync(0xffffffffu, *failed != 0)) {
+                    const uint32_t d = tmem + (uint32_t)(tb * g.N);
+                    const uint64_t toff = (uint64_t)(tt * g.TS);
+#pragma unroll
+                    for (int kh = 0; kh < 9; ++kh)
+                        if (kh < p.KH) {
+                            // (0, 0) first: it writes all N columns
+                            s_mma_lane0(d, ad0[kh][0] + toff, bd0 + (uint64_t)(2 * kh) * bstep,
+                                        g.idesc, kh, (uint32_t)lane);
+                            if (g.N1 > 0)
+                                s_mma_lane0(d, ad0[kh][1] + toff,
+                                            bd0 + (uint64_t)(2 * kh + 1) * bstep, g.idesc1, 1,
+                                            (uint32_t)lane);
+                        }
+                }
+                s_commit_lane0(bar_full + 8u * tb, (uint32_t)lane);
+            }
+            s_commit_lane0(bar_free + 8u * ub, (uint32_t)lane);
         }
-        __syncwarp();
     } else {
         // ------------- staging and tensor-memory drain (warps 0-7) -------------
         // Chunk c's weights into weight buffer bsel.  First the chunk's raw
