@@ -17,29 +17,30 @@
 //    zero outside the image: its rows back to back, one 16-byte entry per
 //    pixel.
 //  - With tap kw + (cpad - pad_w) = 2j + ph, output column p reads entry
-//    p + j.  A row r (the MMA's M = 128 rows) is one entry; the two K
-//    halves of an MMA (K = 16) are entries r and r + 1 of one array, i.e.
-//    the shifts j = 2i and 2i + 1; N holds the NN output channels of each
-//    shift pair i (N = Jb * NN, Jb = ceil(J / 2)).  Per kernel row kh there
-//    is one MMA per phase ph (array (ph, kh & 1), ring row offset kh >> 1):
-//      D[r][i*NN + n] += sum_{h, c} A[r + h][c] * w[n, c, kh, 2(2i + h) + ph - dc]
+//    p + j of phase ph.  A row r (the MMA's M = 128 rows) is one entry; the
+//    two K halves of an MMA (K = 16) are that entry's two phases, arrays
+//    (0, s) and (1, s) (the descriptor's leading byte offset is the distance
+//    between them); N holds the NN output channels of each column shift j
+//    (N = J * NN).  Per kernel row kh there is one MMA (arrays (ph, kh & 1),
+//    ring row offset kh >> 1):
+//      D[r][j*NN + n] += sum_{ph, c} A_ph[r][c] * w[n, c, kh, 2j + ph - dc]
 //    (dc = cpad - pad_w; zero weights outside the kernel or n's group).
-//    Output column p is the sum over i of D[p + 2i][i*NN + n]: the Jb
+//    Output column p is the sum over j of D[p + j][j*NN + n]: the J
 //    accumulator blocks of a row are read once from tensor memory and the
 //    shifted ones added with warp shuffles.  Each staged entry is read by
-//    the tensor core twice per kernel row instead of once per tap.
+//    the tensor core once per kernel row instead of once per tap.
 //  - Entries of consecutive output rows follow each other in the arrays
 //    (ring row i + 1 is the next output row), so a tile is 128 consecutive
 //    entries of the band, whichever rows they belong to; tiles advance by
-//    TS = 128 - 2(Jb - 1) entries so every output finds its shifted rows
-//    in one tile.  Row entries E = OWt + 2 Jb - 1 per output row.
-//  - One CTA per SM: eight warps stage (one thread issues the TMA boxes;
-//    all stage the chunk's weights when the chunk changes) and drain tensor
-//    memory, the two warpgroups taking alternate tiles; four warps issue the
-//    MMAs of every fourth tile (one thread issues an MMA every ~100 cycles
-//    at best).  Two unit buffers and eight tensor-memory tile buffers keep
-//    the tensor core fed while the next unit is staged and earlier tiles
-//    are drained.
+//    TS = 128 - (J - 1) entries so every output finds its shifted rows in
+//    one tile.  Row entries E = OWt + J - 1 per output row.
+//  - One CTA per SM: eight warps stage (all stage the chunk's weights when
+//    the chunk changes) and drain tensor memory, the two warpgroups taking
+//    alternate tiles; one warp issues the input boxes and three warps issue
+//    the MMAs of every third tile (one warp issues an MMA every ~74 cycles
+//    at best, the tensor core takes one of N = 80 every ~52 cycles).  Two
+//    unit buffers and six tensor-memory tile buffers keep the tensor core
+//    fed while the next unit is staged and earlier tiles are drained.
 //  - Every mbarrier wait is bounded; a wait that gives up marks the CTA
 //    failed, its outputs are written as NaN, and before exiting the CTA
 //    waits (bounded) for its copies and MMAs in flight before it frees its
@@ -54,36 +55,35 @@
 namespace gconv {
 namespace {
 
-constexpr int kSWarps = 8;                   // staging + drain
+constexpr int kSWarps = 16;                  // staging + drain
 constexpr int kSProducers = 32 * kSWarps;
+constexpr int kSDrainGroups = kSWarps / 4;   // warpgroups that drain tiles in turn
 constexpr int kSIssuers = 3;                 // MMA issue warps
 constexpr int kSLoader = kSWarps + kSIssuers;   // the warp that issues the input boxes
 constexpr int kSThreads = kSProducers + 32 * (kSIssuers + 1);
-constexpr int kSMaxJb = 3;                   // shift pairs (KW <= 9)
-constexpr int kSMaxNN = 16;                  // output channels per chunk
-constexpr int kSTileBufs = 8;                // tensor-memory tile buffers (N <= 48: 384 columns)
+constexpr int kSMaxJ = 5;                    // column shifts (KW <= 9)
+constexpr int kSTileBufs = 6;                // tensor-memory tile buffers (N <= 80: 480 columns)
 constexpr int kSSmemCap = 220 * 1024;
 constexpr uint32_t kSSpinLimit = 1u << 22;
 // Exchange rows between the warps of a warpgroup: [warpgroup][tile parity]
-// [warp][lane < 4][(i - 1) * NN + c], lanes kSLane floats apart so the four
+// [warp][lane < 4][(j - 1) * NN + c], lanes kSLane floats apart so the four
 // writers (and readers) of a 16-byte vector hit different banks.
-template <int NNT> constexpr int kSLane = (kSMaxJb - 1) * NNT + 4;
-constexpr int kSXchFloats = 2 * 2 * 4 * 4 * kSLane<16>;
+template <int NNT> constexpr int kSLane = (kSMaxJ - 1) * NNT + 4;
+constexpr int kSXchFloats = kSDrainGroups * 2 * 4 * 4 * kSLane<16>;
 
 struct TcsGeom {
-    int NN, J, Jb, N;      // chunk outputs, column shifts, shift pairs, MMA N (16 | N)
-    int N1;                // MMA N of the ph = 1 MMAs (fewer pairs hold taps; 0: none)
+    int NN, J, N;          // chunk outputs, column shifts, MMA N (16 | N)
     int dc, cpad;          // cpad - pad_w (0 or 1), pad_w rounded up to even
     int Bo, OWt, E, TS, Tn, R, R_load, Lv;
     int chunks, bands, cts, units, ctas;
     int arr_bytes;         // one (ph, s) array, 128-byte aligned
     int ring_bytes;        // the four arrays of one unit buffer
-    int b_bytes;           // one weight buffer (KH x 2 phases)
+    int b_bytes;           // one weight buffer (KH blocks)
     int raw_elems;         // the chunk's weights: NN x Cin_g x KH x KW
     int w_dense;           // weights dense and 16-byte aligned per chunk
     int ring_off[2], b_off[2], x_off, bias_off, bar_off, smem;
     int tmem_cols;
-    uint32_t idesc, idesc1;
+    uint32_t idesc;
     FastDiv Ediv, Ndiv;
     int nn_shift, cout_shift;   // log2(NN), log2(Cout_g)
     int vec_store;
@@ -119,18 +119,14 @@ bool tcs_geometry(const Params &p, TcsGeom &g) {
     g.dc = p.pbw & 1;
     g.cpad = p.pbw + g.dc;
     g.J = (p.KW + g.dc + 1) / 2;
-    g.Jb = (g.J + 1) / 2;
-    if (g.Jb > kSMaxJb) return false;
-    g.N = (g.Jb * g.NN + 15) / 16 * 16;
-    // Phase 1 taps kw = 2j + 1 - dc: the last pair holding one may come sooner.
-    const int jmax1 = (p.KW - 2 + g.dc) / 2;   // -1 (none) when KW - 2 + dc < 0
-    g.N1 = p.KW - 2 + g.dc < 0 ? 0 : ((jmax1 / 2 + 1) * g.NN + 15) / 16 * 16;
-    g.TS = 128 - 2 * (g.Jb - 1);
+    if (g.J > kSMaxJ) return false;
+    g.N = (g.J * g.NN + 15) / 16 * 16;
+    g.TS = 128 - (g.J - 1);
     // Column tiles of at most 120 outputs; rows per unit as many (<= 8) as fit.
     g.cts = (p.OW + 119) / 120;
     g.OWt = (p.OW + g.cts - 1) / g.cts;
-    g.E = g.OWt + 2 * g.Jb - 1;   // an output's last pair reads entry p + 2 Jb - 1
-    g.b_bytes = (p.KH * 2 * g.N * 32 + 127) / 128 * 128;
+    g.E = g.OWt + g.J - 1;   // an output's last shift reads entry p + J - 1
+    g.b_bytes = (p.KH * g.N * 32 + 127) / 128 * 128;
     g.raw_elems = g.NN * p.Cin_g * p.KH * p.KW;
     const int x_bytes = (g.raw_elems * 2 > kSXchFloats * 4 ? g.raw_elems * 2 : kSXchFloats * 4);
     const int fixed = 2 * g.b_bytes + (x_bytes + 127) / 128 * 128 + 2 * 16 * 4 + 256;
@@ -175,7 +171,6 @@ bool tcs_geometry(const Params &p, TcsGeom &g) {
     if (pow2 > 512) return false;
     g.tmem_cols = pow2;
     g.idesc = s_idesc(p.dtype == GCONV_BF16, 128, g.N);
-    g.idesc1 = s_idesc(p.dtype == GCONV_BF16, 128, g.N1 > 0 ? g.N1 : 16);
     g.Ediv = FastDiv((uint32_t)g.E);
     g.Ndiv = FastDiv((uint32_t)g.N);
     g.w_dense = 0;
@@ -386,7 +381,7 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         }
         for (int i = 0; i < kSTileBufs; ++i) {
             mbar_init(bar_full + 8u * i, 1);
-            mbar_init(bar_empty + 8u * i, kSProducers / 2);
+            mbar_init(bar_empty + 8u * i, kSProducers / kSDrainGroups);
         }
         *failed = 0;
         fence_barrier_init();
@@ -436,20 +431,18 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
             }
             s_wait_warp(bar_staged + 8u * ub, (uint32_t)((k >> 1) & 1), failed);
             s_fence_after();
-            // Descriptors of (kh, ph)'s operands for tile 0: A from array
-            // (ph, kh & 1) at ring row kh >> 1, its second K half one entry
-            // on (leading byte offset 16); tile tt adds tt * TS entries to
-            // A's start address, the descriptor's low field in 16-byte units
-            // (no carry: shared addresses stay below 2^18).
+            // Descriptors of kh's operands for tile 0: A from array (0, kh & 1)
+            // at ring row kh >> 1, its second K half (phase 1) in array
+            // (1, kh & 1), two arrays on (leading byte offset); tile tt adds
+            // tt * TS entries to A's start address, the descriptor's low field
+            // in 16-byte units (no carry: shared addresses stay below 2^18).
             const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
-            uint64_t ad0[9][2];
+            uint64_t ad0[9];
 #pragma unroll
             for (int kh = 0; kh < 9; ++kh)
-#pragma unroll
-                for (int ph = 0; ph < 2; ++ph)
-                    ad0[kh][ph] = s_desc(ring + (uint32_t)((ph * 2 + (kh & 1)) * g.arr_bytes) +
-                                             (uint32_t)((kh >> 1) * g.E * 16),
-                                         16, 128);
+                ad0[kh] = s_desc(ring + (uint32_t)((kh & 1) * g.arr_bytes) +
+                                     (uint32_t)((kh >> 1) * g.E * 16),
+                                 (uint32_t)(2 * g.arr_bytes), 128);
             const uint64_t bd0 = s_desc(sbase + (uint32_t)g.b_off[bsel], 128, 256);
             const uint64_t bstep = (uint64_t)(g.N * 32 / 16);
             for (int tt = 0; tt < g.Tn; ++tt, ++gt) {
@@ -463,15 +456,9 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                     const uint64_t toff = (uint64_t)(tt * g.TS);
 #pragma unroll
                     for (int kh = 0; kh < 9; ++kh)
-                        if (kh < p.KH) {
-                            // (0, 0) first: it writes all N columns
-                            s_mma_lane0(d, ad0[kh][0] + toff, bd0 + (uint64_t)(2 * kh) * bstep,
-                                        g.idesc, kh, (uint32_t)lane);
-                            if (g.N1 > 0)
-                                s_mma_lane0(d, ad0[kh][1] + toff,
-                                            bd0 + (uint64_t)(2 * kh + 1) * bstep, g.idesc1, 1,
-                                            (uint32_t)lane);
-                        }
+                        if (kh < p.KH)
+                            s_mma_lane0(d, ad0[kh] + toff, bd0 + (uint64_t)kh * bstep, g.idesc,
+                                        kh, (uint32_t)lane);
                 }
                 s_commit_lane0(bar_full + 8u * tb, (uint32_t)lane);
             }
@@ -481,19 +468,19 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         // ------------- staging and tensor-memory drain (warps 0-7) -------------
         // Chunk c's weights into weight buffer bsel.  First the chunk's raw
         // weights [NN][Cin_g][KH][KW] into shared memory (16-byte loads when
-        // they are dense and aligned), then the operand: block (kh, ph) is an
-        // N x 16 K-major matrix whose row n = i*NN + n' (output channel
-        // c*NN + n') holds at K = h*8 + cc the weight of chunk channel cc at
-        // kernel column 2(2i + h) + ph - dc, zero outside the kernel and
-        // outside n''s group.  The raw copy shares the exchange buffer
+        // they are dense and aligned), then the operand: block kh is an
+        // N x 16 K-major matrix whose row n = j*NN + n' (output channel
+        // c*NN + n') holds at K = ph*8 + cc the weight of chunk channel cc at
+        // kernel column 2j + ph - dc, zero outside the kernel and outside
+        // n''s group.  The raw copy shares the exchange buffer
         // (every producer is inside stage() here).
         auto stage_b = [&](int c, int bsel) {
             T *raw = reinterpret_cast<T *>(xch);
             if (g.w_dense) {
-                // at most 16 x 8 x 81 / 8 = 1296 vectors: six per thread, all
-                // loads in flight before the stores
+                // at most 16 x 8 x 81 / 8 = 1296 vectors, all of a thread's
+                // loads in flight before its stores
                 const uint4 *src = reinterpret_cast<const uint4 *>(w + (int64_t)c * g.raw_elems);
-                constexpr int kV = 6;
+                constexpr int kV = (1296 + kSProducers - 1) / kSProducers;
                 uint4 v[kV];
 #pragma unroll
                 for (int i = 0; i < kV; ++i) {
@@ -518,19 +505,17 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
             }
             s_producer_sync();
             unsigned char *bsm = s_smem + g.b_off[bsel];
-            const int rows = p.KH * 2 * g.N;
+            const int rows = p.KH * g.N;
             for (int row = t; row < rows; row += kSProducers) {
-                const int kp = (int)g.Ndiv.div((uint32_t)row);   // 2 kh + ph
-                const int kh = kp >> 1, ph = kp & 1;
-                const int n = row - kp * g.N;
-                const int i = n >> g.nn_shift, np = n & (g.NN - 1);
+                const int kh = (int)g.Ndiv.div((uint32_t)row);
+                const int n = row - kh * g.N;
+                const int j = n >> g.nn_shift, np = n & (g.NN - 1);
                 const int cb = (np >> g.cout_shift) * p.Cin_g;
-                unsigned char *dst = bsm + kp * g.N * 32 + (n >> 3) * 256 + (n & 7) * 16;
+                unsigned char *dst = bsm + kh * g.N * 32 + (n >> 3) * 256 + (n & 7) * 16;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int j = 2 * i + h;
+                for (int ph = 0; ph < 2; ++ph) {
                     const int kw = 2 * j + ph - g.dc;
-                    const bool kw_ok = i < g.Jb && j < g.J && kw >= 0 && kw < p.KW;
+                    const bool kw_ok = j < g.J && kw >= 0 && kw < p.KW;
                     float v[8];
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc) {
@@ -544,7 +529,7 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                     o.y = pack2(v[2], v[3], (T *)nullptr);
                     o.z = pack2(v[4], v[5], (T *)nullptr);
                     o.w = pack2(v[6], v[7], (T *)nullptr);
-                    *reinterpret_cast<uint4 *>(dst + h * 128) = o;
+                    *reinterpret_cast<uint4 *>(dst + ph * 128) = o;
                 }
             }
         };
@@ -575,69 +560,78 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
             ubsel_bits = (ubsel_bits & ~(1 << ub)) | (bsel << ub);
         };
 
-        // Drain tile tt of unit u (global tile gt): warpgroup gt & 1 takes
-        // it (the two warpgroups drain alternate tiles).  Warp qd reads its
-        // 32 accumulator rows, all NN columns of every shift pair i, adds
-        // the rows 2i below (shuffles inside the warp, the next warp's first
-        // rows through shared memory), the bias, rounds once and stores 2 * NN
-        // bytes per output pixel.
+        // Drain tile tt of unit u (global tile gt): warpgroup gt % 4 takes
+        // it (the warpgroups drain tiles in turn).  Warp qd reads its 32
+        // accumulator rows two column blocks at a time and adds block j of
+        // the row j below (a shuffle inside the warp); lanes 0..J-2 leave
+        // their blocks for the warp above, whose last lanes add them after
+        // the warpgroup's barrier.  Then the bias, one rounding and 2 * NN
+        // bytes stored per output pixel.
         const int qd = warp & 3, wg = warp >> 2;
         auto drain = [&](const TcsUnit &u, int k, int tt, int gt) {
             const int ub = k & 1;
             const int tb = gt % kSTileBufs;
             s_wait(bar_full + 8u * tb, (uint32_t)((gt / kSTileBufs) & 1), failed);
             s_fence_after();
-            float a[kSMaxJb][NNT];
             const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(tb * g.N);
-#pragma unroll
-            for (int i = 0; i < kSMaxJb; ++i)
-                if (i < g.Jb) s_ld<NNT>(taddr + (uint32_t)(i * NNT), a[i]);
-            s_wait_ld();
-            s_fence_before();
-            s_arrive(bar_empty + 8u * tb);
-            // Row m < 2 (Jb - 1) of this warp is read at pair i (2i > m) by
-            // row m - 2i + 32 of the warp above: lane m stores those pairs.
             constexpr int kLane = kSLane<NNT>;
             constexpr int kXW = 4 * kLane;   // floats per warp
-            float *xw = xch + ((wg * 2 + ((gt >> 1) & 1)) * 4 + qd) * kXW;
-            if (lane < 2 * (g.Jb - 1)) {
-#pragma unroll
-                for (int i = 1; i < kSMaxJb; ++i)
-                    if (i < g.Jb && 2 * i > lane) {
-#pragma unroll
-                        for (int c4 = 0; c4 < NNT / 4; ++c4)
-                            *reinterpret_cast<float4 *>(xw + lane * kLane + (i - 1) * NNT + 4 * c4) =
-                                make_float4(a[i][4 * c4], a[i][4 * c4 + 1], a[i][4 * c4 + 2],
-                                            a[i][4 * c4 + 3]);
-                    }
-            }
-            s_group_sync(wg);
-            const float *xn = xw + kXW;   // the next warp of the group (qd + 1)
+            float *xw = xch + ((wg * 2 + ((gt / kSDrainGroups) & 1)) * 4 + qd) * kXW;
             float acc[NNT];
 #pragma unroll
-            for (int c = 0; c < NNT; ++c) acc[c] = a[0][c];
+            for (int j0 = 0; j0 < kSMaxJ; j0 += 2) {
+                if (j0 >= g.J) break;
+                float blk[2][NNT];
+                s_ld<NNT>(taddr + (uint32_t)(j0 * NNT), blk[0]);
+                if (j0 + 1 < g.J) s_ld<NNT>(taddr + (uint32_t)((j0 + 1) * NNT), blk[1]);
+                s_wait_ld();
 #pragma unroll
-            for (int i = 1; i < kSMaxJb; ++i) {
-                if (i >= g.Jb) break;
-                float sh[NNT];
+                for (int h = 0; h < 2; ++h) {
+                    const int j = j0 + h;
+                    if (j >= g.J || j >= kSMaxJ) break;
+                    if (j == 0) {
 #pragma unroll
-                for (int c = 0; c < NNT; ++c) sh[c] = __shfl_down_sync(0xffffffffu, a[i][c], 2 * i);
-                if (lane + 2 * i >= 32) {   // the row lies in the next warp (or past the tile)
-                    const int m = lane + 2 * i - 32;
+                        for (int c = 0; c < NNT; ++c) acc[c] = blk[0][c];
+                        continue;
+                    }
+                    // row m < j of this warp is read at shift j by row
+                    // m - j + 32 of the warp above
+                    if (lane < j) {
 #pragma unroll
-                    for (int c4 = 0; c4 < NNT / 4; ++c4) {
-                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (qd < 3)
-                            v = *reinterpret_cast<const float4 *>(xn + m * kLane + (i - 1) * NNT +
-                                                                  4 * c4);
-                        sh[4 * c4] = v.x;
-                        sh[4 * c4 + 1] = v.y;
-                        sh[4 * c4 + 2] = v.z;
-                        sh[4 * c4 + 3] = v.w;
+                        for (int c4 = 0; c4 < NNT / 4; ++c4)
+                            *reinterpret_cast<float4 *>(xw + lane * kLane + (j - 1) * NNT + 4 * c4) =
+                                make_float4(blk[h][4 * c4], blk[h][4 * c4 + 1], blk[h][4 * c4 + 2],
+                                            blk[h][4 * c4 + 3]);
+                    }
+                    const bool inside = lane + j < 32;
+#pragma unroll
+                    for (int c = 0; c < NNT; ++c) {
+                        const float v = __shfl_down_sync(0xffffffffu, blk[h][c], j);
+                        acc[c] += inside ? v : 0.f;
                     }
                 }
+            }
+            s_fence_before();
+            s_arrive(bar_empty + 8u * tb);
+            s_group_sync(wg);
+            // the last lanes: rows of the next warp (none past the tile)
+            if (qd < 3 && lane + g.J - 1 >= 32) {
+                const float *xn = xw + kXW;   // the next warp of the group (qd + 1)
 #pragma unroll
-                for (int c = 0; c < NNT; ++c) acc[c] += sh[c];
+                for (int j = 1; j < kSMaxJ; ++j) {
+                    if (j >= g.J) break;
+                    if (lane + j < 32) continue;
+                    const int m = lane + j - 32;
+#pragma unroll
+                    for (int c4 = 0; c4 < NNT / 4; ++c4) {
+                        const float4 v =
+                            *reinterpret_cast<const float4 *>(xn + m * kLane + (j - 1) * NNT + 4 * c4);
+                        acc[4 * c4] += v.x;
+                        acc[4 * c4 + 1] += v.y;
+                        acc[4 * c4 + 2] += v.z;
+                        acc[4 * c4 + 3] += v.w;
+                    }
+                }
             }
             const int r = 32 * qd + lane;
             const int vpos = tt * g.TS + r;
@@ -680,7 +674,7 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         for (int k = 0; k < nunits; ++k) {
             if (k + 1 < nunits) stage(nxt, k + 1);
             for (int tt = 0; tt < g.Tn; ++tt, ++gt)
-                if ((gt & 1) == wg) drain(cur, k, tt, gt);
+                if (gt % kSDrainGroups == wg) drain(cur, k, tt, gt);
             cur = nxt;
             nxt.next(g, p.N);
         }
