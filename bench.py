@@ -212,6 +212,7 @@ KERNEL_SOURCES = {
     "dw_row8": ["k_row8.cuh", "k_row8.cu", "stencil_math.cuh", "device_common.cuh", "tma.cuh",
                 "launch.cuh"],
     "dw_flat": ["k_flat.cu", "device_common.cuh", "launch.cuh"],
+    "dw_small": ["k_small.cu", "device_common.cuh", "launch.cuh"],
     "dw_mult": ["k_mult.cuh", "k_mult.cu", "device_common.cuh", "tma.cuh", "launch.cuh"],
     "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh", "launch.cuh"],
     "grp_reduce": ["k_reduce.cu", "device_common.cuh", "launch.cuh"],

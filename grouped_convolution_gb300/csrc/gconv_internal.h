@@ -50,6 +50,7 @@ extern const Schedule kGrpPlane;
 extern const Schedule kGrpReduce;
 extern const Schedule kGrpTc;
 extern const Schedule kDwLine;
+extern const Schedule kDwSmall;
 
 // The plain forward convolution of the direct-stencil envelope (dilation 1,
 // not transposed): the only calls the specialised schedules take.

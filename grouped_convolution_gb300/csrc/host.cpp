@@ -31,7 +31,7 @@ std::atomic<uint64_t> g_launches{0};
 thread_local int32_t t_last_cuda_error = 0;
 
 const Schedule *const kSchedules[GCONV_SCHED_COUNT] = {
-    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc, &kDwLine};
+    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc, &kDwLine, &kDwSmall};
 
 int32_t schedule_from_string(const char *s) {
     if (!s || !*s) return GCONV_SCHED_AUTO;
@@ -402,7 +402,8 @@ gconv_status grad_input_shape_and_stride(const gconv_desc *d, int32_t *rank,
 }
 
 // The per-shape picker.  Specialised schedules win where they apply; the
-// fallback schedule dw_flat takes everything else.  Grouped calls the
+// fallback schedule dw_flat takes everything else.  Small NCHW depthwise
+// problems run on dw_small.  Grouped calls the
 // tensor cores can take (4 or 8 channels per group, channels-last 16-bit)
 // run there.  Channels-last depthwise calls outside dw_row8's reach (1-D,
 // non-square or larger kernels, dilation other than 2 on a stride-1 3x3,
@@ -411,6 +412,11 @@ gconv_status grad_input_shape_and_stride(const gconv_desc *d, int32_t *rank,
 // than 152 SMs x 512) and a long tap loop split the taps across lanes.
 static int32_t pick(const gconv_desc &d, const Ptrs &p) {
     const bool dw = d.Cin_g == 1;
+    // Depthwise NCHW problems of at most 2^20 outputs: one wave of threads
+    // without a staging ring (its fill and drain cost more than the work).
+    if (dw && d.layout == GCONV_LAYOUT_NCHW &&
+        (double)d.N * d.C_out * d.OH * d.OW <= (double)(1 << 20) && kDwSmall.supports(d, p))
+        return GCONV_SCHED_DW_SMALL;
     if (dw && d.Cout_g == 1 && kDwRow8.supports(d, p)) return GCONV_SCHED_DW_ROW8;
     if (dw && kDwMult.supports(d, p)) return GCONV_SCHED_DW_MULT;
     if (!dw && kGrpTc.supports(d, p)) return GCONV_SCHED_GRP_TC;

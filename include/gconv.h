@@ -130,7 +130,11 @@ typedef enum gconv_schedule {
     GCONV_SCHED_DW_LINE = 6,     /* channels-last depthwise (multiplier 1), any kernel shape,
                                     stride and dilation, forward or transposed: a thread per
                                     16-byte channel vector and strip of output pixels */
-    GCONV_SCHED_COUNT = 7
+    GCONV_SCHED_DW_SMALL = 7,    /* depthwise (any multiplier, layout, stride, dilation),
+                                    forward: one pass, a thread per 4 outputs of a row, no
+                                    shared memory; picked for NCHW problems of <= 2^20
+                                    outputs */
+    GCONV_SCHED_COUNT = 8
 } gconv_schedule;
 
 typedef enum gconv_layout {

@@ -213,6 +213,35 @@ def test_force_schedule_rules():
     gc.conv_force_schedule("auto")
 
 
+def test_picker_on_the_benchmark_workloads():
+    # The picker's schedule for every benchmark workload at full size: the
+    # small NCHW depthwise layer runs in one pass (dw_small); the larger ones
+    # keep their staged schedules.
+    want = {"dw3x3_f32_nchw": "dw_small", "mbv2_dw3x3_s1_bf16_cl": "dw_row8",
+            "mbv2_dw3x3_s2_bf16_cl": "dw_row8", "dw7x7_bf16_cl": "dw_row8",
+            "dw4x4_m4_f16_nchw": "dw_mult", "grp4x8_9x9_s2_bf16_cl": "grp_tc"}
+    for name, sched in want.items():
+        wl = WORKLOADS[name]
+        xs = cl_strides(wl.N, wl.C_in, wl.H, wl.W) if wl.channels_last else None
+        d = bind(x=((wl.N, wl.C_in, wl.H, wl.W), xs),
+                 w=((wl.C_out, wl.C_in // wl.groups, wl.KH, wl.KW), None),
+                 b=((wl.C_out,), None) if wl.bias else None, stride=tuple(wl.stride),
+                 pb=tuple(wl.pad_before), pa=tuple(wl.pad_after), dil=tuple(wl.dilation),
+                 groups=wl.groups, dtype=wl.torch_dtype.__str__().split(".")[1])
+        got = gc.conv_select_schedule(d, FAKE, FAKE, FAKE if wl.bias else None, FAKE)
+        assert got == sched, (name, got)
+
+
+def test_dw_small_takes_depthwise_only():
+    d = bind(x=((2, 8, 9, 11), None), w=((24, 1, 3, 3), None), groups=8)   # multiplier 3
+    assert gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE) == "dw_small"
+    d.schedule = gc.SCHEDULES["dw_small"]
+    assert gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE) == "dw_small"
+    d = bind(x=((1, 8, 8, 8), None), w=((8, 2, 3, 3), None), groups=4)     # Cin_g 2
+    d.schedule = gc.SCHEDULES["dw_small"]
+    assert status_of(lambda: gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE)) == ERR["SCHEDULE"]
+
+
 def test_dw_forward_refuses_grouped():
     d = bind(x=((1, 8, 8, 8), None), w=((8, 2, 3, 3), None), groups=4)
     assert status_of(lambda: gc.conv_dw_forward(d, FAKE, FAKE, None, FAKE, 0)) == ERR["UNSUPPORTED"]

@@ -49,7 +49,7 @@ GEOMS = [
 ]
 
 DTYPES = ["f32", "f16", "bf16"]
-SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc"]
+SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc", "dw_small"]
 
 
 def workload(g, dtype, cl, bias, seed):
