@@ -86,7 +86,7 @@ struct TcsGeom {
     uint32_t idesc;
     FastDiv Ediv, Ndiv;
     int nn_shift, cout_shift;   // log2(NN), log2(Cout_g)
-    int vec_store;
+    int vec_store;         // 0: element stores, 1: 16-byte, 2: 32-byte vectors
 };
 
 // 64-bit shared-memory matrix descriptor (tcgen05): K-major, no swizzle;
@@ -649,7 +649,16 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
             const int co0 = u.c * NNT;
             T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)oh * p.ys[2] + (int64_t)ow * p.ys[3] +
                     (int64_t)co0 * p.ys[1];
-            if (g.vec_store) {
+            if (NNT == 16 && g.vec_store == 2) {
+                // one 32-byte store: the pixel's whole sector
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = pack2(f[2 * i], f[2 * i + 1], (T *)nullptr);
+                asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(yp),
+                             "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]),
+                             "r"(o[6]), "r"(o[7])
+                             : "memory");
+            } else if (g.vec_store) {
 #pragma unroll
                 for (int v8 = 0; v8 < NNT / 8; ++v8) {
                     uint4 o;
@@ -756,6 +765,10 @@ cudaError_t tcs_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *laun
     // 16-byte stores of 8 output channels
     g.vec_store = aligned(q.y, 16) && p.ys[1] == 1 && p.ys[3] % 8 == 0 && p.ys[2] % 8 == 0 &&
                   p.ys[0] % 8 == 0;
+    // 32-byte stores of 16 output channels
+    if (g.vec_store && g.NN == 16 && aligned(q.y, 32) && p.ys[3] % 16 == 0 &&
+        p.ys[2] % 16 == 0 && p.ys[0] % 16 == 0)
+        g.vec_store = 2;
     if (p.dtype == GCONV_BF16) return tcs_launch_t<__nv_bfloat16>(p, q, s, g);
     return tcs_launch_t<__half>(p, q, s, g);
 }
