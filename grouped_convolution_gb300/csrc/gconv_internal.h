@@ -51,6 +51,7 @@ extern const Schedule kGrpReduce;
 extern const Schedule kGrpTc;
 extern const Schedule kDwLine;
 extern const Schedule kDwSmall;
+extern const Schedule kDwTc;
 
 // The plain forward convolution of the direct-stencil envelope (dilation 1,
 // not transposed): the only calls the specialised schedules take.

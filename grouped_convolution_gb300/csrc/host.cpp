@@ -31,7 +31,7 @@ std::atomic<uint64_t> g_launches{0};
 thread_local int32_t t_last_cuda_error = 0;
 
 const Schedule *const kSchedules[GCONV_SCHED_COUNT] = {
-    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc, &kDwLine, &kDwSmall};
+    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc, &kDwLine, &kDwSmall, &kDwTc};
 
 int32_t schedule_from_string(const char *s) {
     if (!s || !*s) return GCONV_SCHED_AUTO;
@@ -403,7 +403,8 @@ gconv_status grad_input_shape_and_stride(const gconv_desc *d, int32_t *rank,
 
 // The per-shape picker.  Specialised schedules win where they apply; the
 // fallback schedule dw_flat takes everything else.  Small NCHW depthwise
-// problems run on dw_small.  Grouped calls the
+// problems run on dw_small; larger NCHW 16-bit depthwise ones at stride 1 on
+// the tensor cores (dw_tc).  Grouped calls the
 // tensor cores can take (4 or 8 channels per group, channels-last 16-bit)
 // run there.  Channels-last depthwise calls outside dw_row8's reach (1-D,
 // non-square or larger kernels, dilation other than 2 on a stride-1 3x3,
@@ -418,6 +419,7 @@ static int32_t pick(const gconv_desc &d, const Ptrs &p) {
         (double)d.N * d.C_out * d.OH * d.OW <= (double)(1 << 20) && kDwSmall.supports(d, p))
         return GCONV_SCHED_DW_SMALL;
     if (dw && d.Cout_g == 1 && kDwRow8.supports(d, p)) return GCONV_SCHED_DW_ROW8;
+    if (dw && kDwTc.supports(d, p)) return GCONV_SCHED_DW_TC;
     if (dw && kDwMult.supports(d, p)) return GCONV_SCHED_DW_MULT;
     if (!dw && kGrpTc.supports(d, p)) return GCONV_SCHED_GRP_TC;
     if (kDwLine.supports(d, p)) return GCONV_SCHED_DW_LINE;

@@ -134,7 +134,11 @@ typedef enum gconv_schedule {
                                     forward: one pass, a thread per 4 outputs of a row, no
                                     shared memory; picked for NCHW problems of <= 2^20
                                     outputs */
-    GCONV_SCHED_COUNT = 8
+    GCONV_SCHED_DW_TC = 8,       /* NCHW bf16 / fp16 depthwise (multiplier 1, 2, 4, 8 or 16)
+                                    at stride 1: input rows times banded weight matrices on
+                                    the tcgen05 tensor cores, fp32 accumulation in tensor
+                                    memory */
+    GCONV_SCHED_COUNT = 9
 } gconv_schedule;
 
 typedef enum gconv_layout {

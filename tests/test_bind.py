@@ -219,7 +219,7 @@ def test_picker_on_the_benchmark_workloads():
     # keep their staged schedules.
     want = {"dw3x3_f32_nchw": "dw_small", "mbv2_dw3x3_s1_bf16_cl": "dw_row8",
             "mbv2_dw3x3_s2_bf16_cl": "dw_row8", "dw7x7_bf16_cl": "dw_row8",
-            "dw4x4_m4_f16_nchw": "dw_mult", "grp4x8_9x9_s2_bf16_cl": "grp_tc"}
+            "dw4x4_m4_f16_nchw": "dw_tc", "grp4x8_9x9_s2_bf16_cl": "grp_tc"}
     for name, sched in want.items():
         wl = WORKLOADS[name]
         xs = cl_strides(wl.N, wl.C_in, wl.H, wl.W) if wl.channels_last else None

@@ -49,7 +49,7 @@ GEOMS = [
 ]
 
 DTYPES = ["f32", "f16", "bf16"]
-SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc", "dw_small"]
+SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc", "dw_small", "dw_tc"]
 
 
 def workload(g, dtype, cl, bias, seed):
@@ -190,6 +190,34 @@ def test_grp_tc_geometry_matches_oracle(case, dtype):
     y = run_gpu(wl, x, w, b, "grp_tc")
     assert y is not None, "grp_tc must take this case"
     RAN["grp_tc"] += 1
+    check(wl, x, w, b, y)
+
+
+# dw_tc (NCHW 16-bit depthwise at stride 1 on the tensor cores) geometry:
+# multipliers 1 to 16, kernels 1x1 to 9x9 (one and two K steps), every pad
+# offset in a chunk, planes taller than a 128-row tile and wider than a unit's
+# 128 columns, ragged last tiles, several channels per CTA.
+DWTC_CASES = [
+    # name, N, Cin_g, Cout_g, G, H, W, KH, KW, stride, pad_before, pad_after
+    # (W a multiple of 8: the input rows are TMA boxes of 16-byte chunks)
+    ("c4_small", 2, 1, 4, 6, 40, 40, 4, 4, (1, 1), (1, 1), (2, 2)),
+    ("m1_k3", 1, 1, 1, 5, 21, 32, 3, 3, (1, 1), (1, 1), (1, 1)),
+    ("m2_k9_tall", 1, 1, 2, 2, 150, 24, 9, 9, (1, 1), (4, 4), (4, 4)),
+    ("m1_wide", 1, 1, 1, 2, 12, 296, 3, 5, (1, 1), (0, 2), (1, 3)),
+    ("m16_k1", 1, 1, 16, 2, 7, 32, 1, 1, (1, 1), (0, 0), (0, 0)),
+    ("m8_k7x2_pad7", 1, 1, 8, 2, 11, 24, 7, 2, (1, 1), (3, 7), (3, 0)),
+    ("m4_many", 3, 1, 4, 64, 19, 24, 3, 3, (1, 1), (1, 1), (1, 1)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("case", DWTC_CASES, ids=[c[0] for c in DWTC_CASES])
+def test_dw_tc_geometry_matches_oracle(case, dtype):
+    wl = workload(case, dtype, False, DWTC_CASES.index(case) % 2 == 0, seed=81 + DWTC_CASES.index(case))
+    x, w, b = make_inputs(wl)
+    y = run_gpu(wl, x, w, b, "dw_tc")
+    assert y is not None, "dw_tc must take this case"
+    RAN["dw_tc"] += 1
     check(wl, x, w, b, y)
 
 
