@@ -30,7 +30,7 @@
 //  - One CTA per SM: eight warps stage the weights and drain tensor memory
 //    (two warpgroups taking alternate tiles), two warps issue the MMAs of
 //    alternate tiles, one warp issues the input boxes.  Two unit buffers
-//    and up to eight tensor-memory tile buffers.
+//    and up to eight tensor-memory tile buffers; three unit buffers.
 //  - Every mbarrier wait is bounded; a wait that gives up marks the CTA
 //    failed, its outputs are written as NaN, and before exiting the CTA
 //    waits (bounded) for its copies and MMAs in flight before it frees its
@@ -54,6 +54,7 @@ constexpr int kDIssuers = 2;                  // MMA issue warps
 constexpr int kDLoader = kDWarps + kDIssuers;   // the warp that issues the input boxes
 constexpr int kDThreads = kDDrain + 32 * (kDIssuers + 1);
 constexpr int kDMaxBufs = 8;                  // tensor-memory tile buffers
+constexpr int kDUnitBufs = 3;                 // unit buffers (input staging ring)
 constexpr int kDMaxTiles = 8;                 // 16-column tiles per unit
 constexpr int kDSmemCap = 220 * 1024;
 
@@ -68,7 +69,7 @@ struct DtcGeom {
     int chunk_bytes;   // one chunk's slot: R rows of 16 bytes, rounded up to 128
     int unit_bytes, b_bytes;
     int units, ctas, bufs, tmem_cols;
-    int ring_off[2], b_off[2], bar_off, smem;
+    int b_off0, bar_off, smem;   // weight buffers at b_off0 + i * b_bytes
     uint32_t idesc;
     int vec_store;     // 32-byte stores of 16 output columns
 };
@@ -92,13 +93,10 @@ bool dwtc_geometry(const Params &p, DtcGeom &g) {
     g.chunk_bytes = (g.R * 16 + 127) / 128 * 128;   // TMA destinations 128-byte aligned
     g.unit_bytes = (g.nch * g.chunk_bytes + 127) / 128 * 128;
     g.b_bytes = (p.KH * g.ksteps * g.N * 32 + 127) / 128 * 128;
-    g.ring_off[0] = 0;
-    g.ring_off[1] = g.unit_bytes;
-    g.b_off[0] = 2 * g.unit_bytes;
-    g.b_off[1] = g.b_off[0] + g.b_bytes;
-    g.bar_off = g.b_off[1] + g.b_bytes;
+    g.b_off0 = kDUnitBufs * g.unit_bytes;   // unit buffer i at i * unit_bytes
+    g.bar_off = g.b_off0 + 2 * g.b_bytes;
     g.bufs = 512 / g.N < kDMaxBufs ? 512 / g.N : kDMaxBufs;
-    g.smem = g.bar_off + 8 * (2 + 2 + 2 * kDMaxBufs + 2) + 16;
+    g.smem = g.bar_off + 8 * (2 * kDUnitBufs + 2 * kDMaxBufs + 2) + 16;
     if (g.smem > kDSmemCap) return false;
     int cols = g.bufs * g.N, pow2 = 32;
     while (pow2 < cols) pow2 *= 2;
@@ -150,16 +148,17 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     const int nunits = per + ((int)blockIdx.x < extra ? 1 : 0);
     if (nunits <= 0) return;
 
-    // mbarriers: staged[2] (a unit's boxes landed), free[2] (every MMA that
+    // mbarriers: staged[3] (a unit's boxes landed), free[3] (every MMA that
     // read the unit buffer completed: one commit per issuer), full[bufs] (a
     // tile's MMAs completed), empty[bufs] (a tile drained: 128 arrivals),
-    // b_ready[2] (a channel's weights written into weight buffer i).
+    // b_ready[2] (a channel's weights written into weight buffer i).  Unit
+    // k uses unit buffer k % 3, in phase (k / 3) & 1.
     const uint32_t bar_staged = sbase + (uint32_t)g.bar_off;
-    const uint32_t bar_free = bar_staged + 16u;
-    const uint32_t bar_full = bar_staged + 32u;
+    const uint32_t bar_free = bar_staged + 8u * kDUnitBufs;
+    const uint32_t bar_full = bar_free + 8u * kDUnitBufs;
     const uint32_t bar_empty = bar_full + 8u * kDMaxBufs;
     const uint32_t bar_bready = bar_empty + 8u * kDMaxBufs;
-    const int slot_off = g.bar_off + 8 * (2 + 2 + 2 * kDMaxBufs + 2);
+    const int slot_off = g.bar_off + 8 * (2 * kDUnitBufs + 2 * kDMaxBufs + 2);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(d_smem + slot_off);
     volatile int *failed = reinterpret_cast<volatile int *>(d_smem + slot_off + 4);
 
@@ -170,11 +169,11 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     if (t == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kDUnitBufs; ++i) {
             mbar_init(bar_staged + 8u * i, 1);
             mbar_init(bar_free + 8u * i, kDIssuers);
-            mbar_init(bar_bready + 8u * i, kDDrain);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(bar_bready + 8u * i, kDDrain);
         for (int i = 0; i < kDMaxBufs; ++i) {
             mbar_init(bar_full + 8u * i, 1);
             mbar_init(bar_empty + 8u * i, kDDrain / 2);
@@ -189,19 +188,20 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     const uint32_t tmem = *tslot;
 
     if (warp == kDLoader) {
-        // ------ input boxes: unit k into unit buffer k & 1 once the tensor
-        // core has read the unit two back; the whole warp runs the loop,
+        // ------ input boxes: unit k into unit buffer k % 3 once the tensor
+        // core has read the unit three back; the whole warp runs the loop,
         // lane 0 issues ------
         const uint32_t unit_tx = (uint32_t)(g.nch * g.R * 16);   // the boxes' bytes
         DtcUnit u;
         u.set(u0, g, p.N);
         for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
-            const int ub = k & 1;
-            if (k >= 2) s_wait_warp(bar_free + 8u * ub, (uint32_t)(((k - 2) >> 1) & 1), failed);
+            const int ub = k % kDUnitBufs;
+            if (k >= kDUnitBufs)
+                s_wait_warp(bar_free + 8u * ub, (uint32_t)((k / kDUnitBufs - 1) & 1), failed);
             s_expect_tx_lane0(bar_staged + 8u * ub, unit_tx, (uint32_t)lane);
             const int col0 = 16 * g.owt * u.gw - p.pbw - g.a;   // a multiple of 8
             const int row0 = 128 * u.ot - p.pbh;
-            const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
+            const uint32_t ring = sbase + (uint32_t)(ub * g.unit_bytes);
             for (int i = 0; i < g.nch; ++i)
                 s_tma_lane0(ring + (uint32_t)(i * g.chunk_bytes), &xmap, bar_staged + 8u * ub,
                             col0 + 8 * i, row0, u.c, u.n, (uint32_t)lane);
@@ -214,17 +214,17 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         u.set(u0, g, p.N);
         int prev_c = -1, bsel = 1, bstaged = 0;   // bit i: phase of b_ready[i]
         for (int k = 0; k < nunits; ++k, u.next(g, p.N)) {
-            const int ub = k & 1;
+            const int ub = k % kDUnitBufs;
             if (u.c != prev_c) {   // the weights of a new channel, in the other buffer
                 prev_c = u.c;
                 bsel ^= 1;
                 s_wait_warp(bar_bready + 8u * bsel, (uint32_t)((bstaged >> bsel) & 1), failed);
                 bstaged ^= 1 << bsel;
             }
-            s_wait_warp(bar_staged + 8u * ub, (uint32_t)((k >> 1) & 1), failed);
+            s_wait_warp(bar_staged + 8u * ub, (uint32_t)((k / kDUnitBufs) & 1), failed);
             s_fence_after();
-            const uint32_t ring = sbase + (uint32_t)g.ring_off[ub];
-            const uint32_t bbase = sbase + (uint32_t)g.b_off[bsel];
+            const uint32_t ring = sbase + (uint32_t)(ub * g.unit_bytes);
+            const uint32_t bbase = sbase + (uint32_t)(g.b_off0 + bsel * g.b_bytes);
             for (int tt = 0; tt < g.owt; ++tt, ++gt) {
                 if (gt % kDIssuers != iss) continue;
                 const int tb = gt % g.bufs;
@@ -256,7 +256,7 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         // holds at K = k the weight of output channel c*m + mm at kernel
         // column 16 s + k - a - jj (zero outside the kernel).
         auto stage_b = [&](int c, int bsel) {
-            unsigned char *bsm = d_smem + g.b_off[bsel];
+            unsigned char *bsm = d_smem + g.b_off0 + bsel * g.b_bytes;
             const int rows = p.KH * g.ksteps * g.N;
             for (int row = t; row < rows; row += kDDrain) {
                 const int blk = row / g.N;
@@ -289,11 +289,12 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         // are through the tensor core; then every drain thread arrives on
         // b_ready of that buffer.
         auto stage = [&](const DtcUnit &u, int k) {
-            const int ub = k & 1;
             if (u.c != prev_c) {
                 prev_c = u.c;
                 bsel ^= 1;
-                if (k >= 2) s_wait(bar_free + 8u * ub, (uint32_t)(((k - 2) >> 1) & 1), failed);
+                if (k >= 2)
+                    s_wait(bar_free + 8u * (uint32_t)((k - 2) % kDUnitBufs),
+                           (uint32_t)(((k - 2) / kDUnitBufs) & 1), failed);
                 stage_b(u.c, bsel);
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
                 s_arrive(bar_bready + 8u * bsel);
@@ -301,49 +302,68 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
         };
 
         // Drain tile tt of unit u (global tile gt): warpgroup gt & 1 takes
-        // it.  Thread r of the warpgroup holds output row 128 ot + r; for
-        // each of the m output channels it reads 16 columns, adds the bias,
-        // rounds once and stores 32 bytes.
+        // it.  Thread r of the warpgroup holds output row 128 ot + r; it
+        // reads the 16 columns of up to four output channels at once, frees
+        // the tile buffer as soon as the last of them is in registers, adds
+        // the bias, rounds once and stores 32 bytes per channel.
         const int qd = warp & 3, wg = warp >> 2;
         auto drain = [&](const DtcUnit &u, int tt, int gt) {
             const int tb = gt % g.bufs;
-            s_wait(bar_full + 8u * tb, (uint32_t)((gt / g.bufs) & 1), failed);
-            s_fence_after();
             const int r = 32 * qd + lane;
             const int oh = 128 * u.ot + r;
             const int ow0 = 16 * (g.owt * u.gw + tt);
             const bool row_ok = oh < p.OH && ow0 < p.OW;
-            const bool bad = *failed != 0;
             const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(tb * g.N);
-            for (int mm = 0; mm < g.m; ++mm) {
-                float v[16];
-                __syncwarp();
-                s_ld<16>(taddr + (uint32_t)(16 * mm), v);   // the whole warp
-                s_wait_ld();
-                if (row_ok) {
-                const int co = u.c * g.m + mm;
-                const float bv = p.has_bias ? load_f32(b + (int64_t)co * p.bs) : 0.f;
+            for (int mb = 0; mb < g.m; mb += 4) {
+                // the bias loads go out before the waits
+                float bv[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = bad ? __int_as_float(0x7fc00000) : v[i] + bv;
-                T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)co * p.ys[1] + (int64_t)oh * p.ys[2] +
-                        (int64_t)ow0 * p.ys[3];
-                if (g.vec_store && ow0 + 16 <= p.OW) {
-                    uint32_t o[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = pack2(v[2 * i], v[2 * i + 1], (T *)nullptr);
-                    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(yp),
-                                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]),
-                                 "r"(o[6]), "r"(o[7])
-                                 : "memory");
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (ow0 + i < p.OW) yp[(int64_t)i * p.ys[3]] = from_f32<T>(v[i]);
+                for (int i = 0; i < 4; ++i)
+                    bv[i] = (p.has_bias && mb + i < g.m)
+                                ? load_f32(b + (int64_t)(u.c * g.m + mb + i) * p.bs)
+                                : 0.f;
+                if (mb == 0) {
+                    s_wait(bar_full + 8u * tb, (uint32_t)((gt / g.bufs) & 1), failed);
+                    s_fence_after();
                 }
+                float v[4][16];
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i)   // the whole warp
+                    if (mb + i < g.m) s_ld<16>(taddr + (uint32_t)(16 * (mb + i)), v[i]);
+                s_wait_ld();
+                if (mb + 4 >= g.m) {   // the tile buffer is read: free it
+                    s_fence_before();
+                    s_arrive(bar_empty + 8u * tb);
+                }
+                if (!row_ok) continue;
+                const bool bad = *failed != 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (mb + i >= g.m) break;
+                    const int co = u.c * g.m + mb + i;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        v[i][e] = bad ? __int_as_float(0x7fc00000) : v[i][e] + bv[i];
+                    T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)co * p.ys[1] +
+                            (int64_t)oh * p.ys[2] + (int64_t)ow0 * p.ys[3];
+                    if (g.vec_store && ow0 + 16 <= p.OW) {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[e] = pack2(v[i][2 * e], v[i][2 * e + 1], (T *)nullptr);
+                        asm volatile(
+                            "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(yp),
+                            "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]),
+                            "r"(o[6]), "r"(o[7])
+                            : "memory");
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (ow0 + e < p.OW) yp[(int64_t)e * p.ys[3]] = from_f32<T>(v[i][e]);
+                    }
                 }
             }
-            s_fence_before();
-            s_arrive(bar_empty + 8u * tb);
         };
 
         DtcUnit cur;
@@ -364,9 +384,10 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
     if (t == 0) {
         const int kl = nunits - 1;
         if (*failed)
-            for (int k = kl > 0 ? kl - 1 : 0; k <= kl; ++k)
-                s_wait_final(bar_staged + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1));
-        s_wait_final(bar_free + 8u * (uint32_t)(kl & 1), (uint32_t)((kl >> 1) & 1));
+            for (int k = kl >= kDUnitBufs - 1 ? kl - (kDUnitBufs - 1) : 0; k <= kl; ++k)
+                s_wait_final(bar_staged + 8u * (uint32_t)(k % kDUnitBufs),
+                             (uint32_t)((k / kDUnitBufs) & 1));
+        s_wait_final(bar_free + 8u * (uint32_t)(kl % kDUnitBufs), (uint32_t)((kl / kDUnitBufs) & 1));
     }
     __syncthreads();
     if (warp == kDWarps)
