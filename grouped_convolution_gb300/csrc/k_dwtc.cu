@@ -223,8 +223,8 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
             }
             s_wait_warp(bar_staged + 8u * ub, (uint32_t)((k / kDUnitBufs) & 1), failed);
             s_fence_after();
-            const uint32_t ring = sbase + (uint32_t)(ub * g.unit_bytes);
-            const uint32_t bbase = sbase + (uint32_t)(g.b_off0 + bsel * g.b_bytes);
+            const uint64_t ad0 = s_desc(sbase + (uint32_t)(ub * g.unit_bytes), (uint32_t)g.chunk_bytes, 128);
+            const uint64_t bd0 = s_desc(sbase + (uint32_t)(g.b_off0 + bsel * g.b_bytes), 128, 256);
             for (int tt = 0; tt < g.owt; ++tt, ++gt) {
                 if (gt % kDIssuers != iss) continue;
                 const int tb = gt % g.bufs;
@@ -233,17 +233,21 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                 s_fence_after();
                 if (!__any_sync(0xffffffffu, *failed != 0)) {
                     const uint32_t d = tmem + (uint32_t)(tb * g.N);
-                    for (int kh = 0; kh < p.KH; ++kh)
-                        for (int s = 0; s < g.ksteps; ++s) {
-                            // A: chunks 2tt + 2s (K 0-7) and the next (K 8-15),
-                            // from staged row kh on
-                            const uint64_t ad = s_desc(
-                                ring + (uint32_t)((2 * tt + 2 * s) * g.chunk_bytes + kh * 16),
-                                (uint32_t)g.chunk_bytes, 128);
-                            const uint64_t bd = s_desc(
-                                bbase + (uint32_t)((kh * g.ksteps + s) * g.N * 32), 128, 256);
-                            s_mma_lane0(d, ad, bd, g.idesc, (kh | s) != 0, (uint32_t)lane);
+                    // A: chunks 2tt + 2s (K 0-7) and the next (K 8-15) from
+                    // staged row kh on; the descriptors' start fields (16-byte
+                    // units, no carry below 2^18 bytes) advance by the offsets
+                    const uint64_t at = ad0 + (uint64_t)((2 * tt * g.chunk_bytes) >> 4);
+#pragma unroll
+                    for (int kh = 0; kh < 9; ++kh) {
+                        if (kh >= p.KH) break;
+#pragma unroll
+                        for (int s = 0; s < 2; ++s) {
+                            if (s >= g.ksteps) break;
+                            s_mma_lane0(d, at + (uint64_t)((2 * s * g.chunk_bytes + kh * 16) >> 4),
+                                        bd0 + (uint64_t)(((kh * g.ksteps + s) * g.N * 32) >> 4),
+                                        g.idesc, (kh | s) != 0, (uint32_t)lane);
                         }
+                    }
                 }
                 s_commit_lane0(bar_full + 8u * tb, (uint32_t)lane);
             }
