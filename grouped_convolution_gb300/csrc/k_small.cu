@@ -47,12 +47,25 @@ cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaSt
 constexpr int kSmallQuad = 4;     // outputs per thread
 constexpr int kSmallThreads = 256;
 
+// Four consecutive outputs rounded and stored at once: y + ow0 is aligned
+// to the quad's size (checked on the host).
+__device__ __forceinline__ void store_quad(float *q, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(q) = make_float4(a, b, c, d);
+}
+template <typename T>
+__device__ __forceinline__ void store_quad(T *q, float a, float b, float c, float d) {
+    uint2 o;
+    o.x = pack2(a, b, (T *)nullptr);
+    o.y = pack2(c, d, (T *)nullptr);
+    *reinterpret_cast<uint2 *>(q) = o;
+}
+
 // Square K x K kernel, stride 1 and dilation 1 along the row (any stride
 // and dilation down the column).
 template <typename T, int K>
 __global__ void __launch_bounds__(kSmallThreads)
 small_kernel_k(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict__ b,
-               T *__restrict__ y, Params p, int quads, int64_t total) {
+               T *__restrict__ y, Params p, int quads, int64_t total, int vec) {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t idx = (int64_t)blockIdx.x * kSmallThreads + threadIdx.x;
@@ -94,9 +107,14 @@ small_kernel_k(const T *__restrict__ x, const T *__restrict__ w, const T *__rest
             for (int i = 0; i < kSmallQuad; ++i) acc[i] = fmaf(wr[kh][kw], win[kh][i + kw], acc[i]);
     const float bv = p.has_bias ? load_f32(b + (int64_t)co * p.bs) : 0.f;
     T *yr = y + (int64_t)n * p.ys[0] + (int64_t)co * p.ys[1] + (int64_t)oh * p.ys[2];
+    if (vec && ow0 + kSmallQuad <= p.OW) {
+        // the quad's 4 outputs in one store (16 bytes fp32, 8 bytes 16-bit)
+        store_quad(yr + ow0, acc[0] + bv, acc[1] + bv, acc[2] + bv, acc[3] + bv);
+    } else {
 #pragma unroll
-    for (int i = 0; i < kSmallQuad; ++i)
-        if (ow0 + i < p.OW) yr[(int64_t)(ow0 + i) * p.ys[3]] = from_f32<T>(acc[i] + bv);
+        for (int i = 0; i < kSmallQuad; ++i)
+            if (ow0 + i < p.OW) yr[(int64_t)(ow0 + i) * p.ys[3]] = from_f32<T>(acc[i] + bv);
+    }
 }
 
 // Any other shape: a loop over the taps.
@@ -175,6 +193,11 @@ cudaError_t small_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *la
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     const bool unit = p.sw == 1 && p.dw == 1;
     const int K = unit && p.KH == p.KW ? p.KH : 0;
+    // one vector store per quad: unit column stride, quads aligned in memory
+    const int qb = kSmallQuad * (int)dtype_size(p.dtype);
+    const int vec = p.ys[3] == 1 && (p.ys[2] * dtype_size(p.dtype)) % qb == 0 &&
+                    (p.ys[1] * dtype_size(p.dtype)) % qb == 0 &&
+                    (p.ys[0] * dtype_size(p.dtype)) % qb == 0 && aligned(q.y, qb);
     return GCONV_DISPATCH_DTYPE(p.dtype, T, [&] {
         const T *x = static_cast<const T *>(q.x);
         const T *w = static_cast<const T *>(q.w);
@@ -183,11 +206,11 @@ cudaError_t small_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *la
         const dim3 grid((unsigned)blocks), block(kSmallThreads);
         cudaError_t e;
         if (K == 3)
-            e = launch_plain(small_kernel_k<T, 3>, grid, block, s, x, w, b, y, p, quads, total);
+            e = launch_plain(small_kernel_k<T, 3>, grid, block, s, x, w, b, y, p, quads, total, vec);
         else if (K == 5)
-            e = launch_plain(small_kernel_k<T, 5>, grid, block, s, x, w, b, y, p, quads, total);
+            e = launch_plain(small_kernel_k<T, 5>, grid, block, s, x, w, b, y, p, quads, total, vec);
         else if (K == 7)
-            e = launch_plain(small_kernel_k<T, 7>, grid, block, s, x, w, b, y, p, quads, total);
+            e = launch_plain(small_kernel_k<T, 7>, grid, block, s, x, w, b, y, p, quads, total, vec);
         else
             e = unit ? launch_plain(small_kernel<T, true>, grid, block, s, x, w, b, y, p, quads, total)
                      : launch_plain(small_kernel<T, false>, grid, block, s, x, w, b, y, p, quads, total);
