@@ -131,8 +131,8 @@ def select(desc, aligned=True):
 
 def test_schedule_selection_wider_envelope():
     # dilation 2, 3x3, stride 1, channels-last depthwise -> dw_row8 (its
-    # dilated ring); other dilated channels-last depthwise -> dw_line; NCHW
-    # dilated -> dw_flat / grp_reduce
+    # dilated ring); other dilated channels-last depthwise -> dw_line; a
+    # small NCHW dilated one -> dw_small (one pass, any dilation)
     d = gc.conv_bind(cl4(8, 64, 20, 20), dense((64, 1, 3, 3)), None, 1, 2, 2, 2, 64,
                      dtype="bfloat16")
     assert select(d) == "dw_row8"
@@ -147,8 +147,8 @@ def test_schedule_selection_wider_envelope():
     assert select(d) == "dw_line"
     d = gc.conv_bind(dense((8, 64, 20, 20)), dense((64, 1, 3, 3)), None, 1, 2, 2, 2, 64,
                      dtype="bfloat16")
-    assert select(d) in ("dw_flat", "grp_reduce")
-    for s in ("dw_row8", "dw_mult", "grp_plane", "grp_tc"):
+    assert select(d) == "dw_small"
+    for s in ("dw_row8", "dw_mult", "grp_plane", "grp_tc", "dw_tc"):
         d.schedule = gc.SCHEDULES[s]
         assert status_of(lambda: select(d)) == ERR["SCHEDULE"]
     # 1-D channels-last depthwise -> dw_line
