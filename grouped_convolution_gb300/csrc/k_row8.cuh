@@ -320,52 +320,67 @@ row8_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ x,
             const uint32_t stage0 = win0 + (uint32_t)(cslot * g.stage);
             // Straight-line over the stage's U rows (no branches around the
             // arithmetic, so the scheduler can overlap the rows' loads):
-            // every row is multiplied into every set it feeds; sets whose
-            // output row lies outside the run collect values that are never
-            // stored, and each set is reset right after its last tap row.
+            // every row is multiplied into every set it feeds; each set is
+            // reset right after its last tap row.  MODE 1 is the run's first
+            // stage and MODE 2 a stage that starts at the run's end: their
+            // taps that feed output rows before the run (MODE 1) or past it
+            // (MODE 2) are left out at compile time; the other stages have
+            // none, and sets whose output row lies outside the run are never
+            // stored.
+            auto stage_body = [&](auto mode) {
+                constexpr int MODE = decltype(mode)::value;
 #pragma unroll
-            for (int ph = 0; ph < U; ++ph) {
-                const int r = r0 + ph;
-                const uint32_t st = stage0 + (uint32_t)(ph * row_bytes);
-                float2 xr[WIN][P];
+                for (int ph = 0; ph < U; ++ph) {
+                    const int r = r0 + ph;
+                    const uint32_t st = stage0 + (uint32_t)(ph * row_bytes);
+                    float2 xr[WIN][P];
 #pragma unroll
-                for (int j = 0; j < WIN; ++j) {
-                    V v;
-                    Lds<VB>::load(v, st + (uint32_t)(j * g.pitch));
-                    widen<T, VEC>(v, xr[j]);
-                }
-#pragma unroll
-                for (int kh = 0; kh < K; ++kh) {
-                    const int d = ph - kh * D;           // (r - kh*D) - r0
-                    if (fmod_pos(d, SH) != 0) continue;  // no output row has tap row kh here
-                    const int set = fmod_pos(fdiv(d, SH), R);
-#pragma unroll
-                    for (int i = 0; i < S; ++i)
-#pragma unroll
-                        for (int kw = 0; kw < K; ++kw)
-#pragma unroll
-                            for (int k = 0; k < P; ++k)   // packed: half the issue slots
-                                fma2_packed(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw * D][k]);
-                }
-                // The output row whose last tap row this was is done.
-                const int d = ph - (KX - 1);
-                if (fmod_pos(d, SH) == 0) {
-                    const int set = fmod_pos(fdiv(d, SH), R);
-                    const int jn = r - (KX - 1);         // SH * output row within the run
-                    if (active && jn >= 0 && jn < run.rows * SH) {
-                        // output row jn / SH = r0 / SH + (ph - K + 1) / SH
-                        T *yrow = ystage + (int64_t)fdiv(ph - (KX - 1), SH) * p.ys[2];
-#pragma unroll
-                        for (int i = 0; i < S; ++i)
-                            if (pix_ok[i])
-                                IO::store(yrow + (int64_t)i * p.ys[3], pack_pairs<T, VEC>(acc[set][i]));
+                    for (int j = 0; j < WIN; ++j) {
+                        V v;
+                        Lds<VB>::load(v, st + (uint32_t)(j * g.pitch));
+                        widen<T, VEC>(v, xr[j]);
                     }
 #pragma unroll
-                    for (int i = 0; i < S; ++i)
+                    for (int kh = 0; kh < K; ++kh) {
+                        const int d = ph - kh * D;           // (r - kh*D) - r0
+                        if (fmod_pos(d, SH) != 0) continue;  // no output row has tap row kh here
+                        if (MODE == 1 && d < 0) continue;    // its output row precedes the run
+                        if (MODE == 2 && d >= 0) continue;   // its output row is past the run
+                        const int set = fmod_pos(fdiv(d, SH), R);
 #pragma unroll
-                        for (int k = 0; k < P; ++k) acc[set][i][k] = bias[k];
+                        for (int i = 0; i < S; ++i)
+#pragma unroll
+                            for (int kw = 0; kw < K; ++kw)
+#pragma unroll
+                                for (int k = 0; k < P; ++k)   // packed: half the issue slots
+                                    fma2_packed(acc[set][i][k], wr[kh][kw][k], xr[i * SW + kw * D][k]);
+                    }
+                    // The output row whose last tap row this was is done.
+                    const int d = ph - (KX - 1);
+                    if (fmod_pos(d, SH) == 0) {
+                        const int set = fmod_pos(fdiv(d, SH), R);
+                        const int jn = r - (KX - 1);         // SH * output row within the run
+                        if (active && jn >= 0 && jn < run.rows * SH) {
+                            // output row jn / SH = r0 / SH + (ph - K + 1) / SH
+                            T *yrow = ystage + (int64_t)fdiv(ph - (KX - 1), SH) * p.ys[2];
+#pragma unroll
+                            for (int i = 0; i < S; ++i)
+                                if (pix_ok[i])
+                                    IO::store(yrow + (int64_t)i * p.ys[3], pack_pairs<T, VEC>(acc[set][i]));
+                        }
+#pragma unroll
+                        for (int i = 0; i < S; ++i)
+#pragma unroll
+                            for (int k = 0; k < P; ++k) acc[set][i][k] = bias[k];
+                    }
                 }
-            }
+            };
+            if (r0 == 0)
+                stage_body(std::integral_constant<int, 1>{});
+            else if (r0 == run.rows * SH)
+                stage_body(std::integral_constant<int, 2>{});
+            else
+                stage_body(std::integral_constant<int, 0>{});
             ystage += (int64_t)R * p.ys[2];   // U / SH output rows per stage
             if (++cslot == g.NS) {
                 cslot = 0;
