@@ -341,14 +341,14 @@ dwtc_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
                     s_arrive(bar_empty + 8u * tb);
                 }
                 if (!row_ok) continue;
-                const bool bad = *failed != 0;
+                const bool bad = *failed != 0;   // poison through the bias: NaN outputs
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (mb + i >= g.m) break;
                     const int co = u.c * g.m + mb + i;
+                    const float bi = bad ? __int_as_float(0x7fc00000) : bv[i];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        v[i][e] = bad ? __int_as_float(0x7fc00000) : v[i][e] + bv[i];
+                    for (int e = 0; e < 16; ++e) v[i][e] += bi;
                     T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)co * p.ys[1] +
                             (int64_t)oh * p.ys[2] + (int64_t)ow0 * p.ys[3];
                     if (g.vec_store && ow0 + 16 <= p.OW) {
