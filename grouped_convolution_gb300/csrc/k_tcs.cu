@@ -499,11 +499,14 @@ tcs_kernel(const __grid_constant__ CUtensorMap xmap, const T *__restrict__ w,
             const bool ok = r < g.TS && vpos < g.Lv && pc < g.OWt && q < g.Bo && oh < p.OH &&
                             ow < p.OW;
             if (!ok) return;
-            const bool bad = *failed != 0;
             const float *bs = bias_s + ((ubsel_bits >> ub) & 1) * 16;
             float f[NNT];
 #pragma unroll
-            for (int c = 0; c < NNT; ++c) f[c] = bad ? __int_as_float(0x7fc00000) : acc[c] + bs[c];
+            for (int c = 0; c < NNT; ++c) f[c] = acc[c] + bs[c];
+            if (*failed != 0) {   // a failed CTA writes NaN
+#pragma unroll
+                for (int c = 0; c < NNT; ++c) f[c] = __int_as_float(0x7fc00000);
+            }
             const int co0 = u.c * NNT;
             T *yp = y + (int64_t)u.n * p.ys[0] + (int64_t)oh * p.ys[2] + (int64_t)ow * p.ys[3] +
                     (int64_t)co0 * p.ys[1];
