@@ -13,11 +13,11 @@
 // GPU that loads the library holds it until the process exits.  Host code
 // cannot pass the array's name to a kernel (in host code it names a host-side
 // stand-in, not device memory), so the device address is looked up with
-// cudaGetSymbolAddress once per device, on the first call made with that
-// device current, and cached.  That first call should come before any stream
-// capture begins.  The cached address stays valid for as long as the device's
-// primary context lives: do not reset the device (cudaDeviceReset) while the
-// library is in use, since a new context may place the array elsewhere.
+// cudaGetSymbolAddress on the first call made in a context and cached with
+// that context.  A call made in another context (after a cudaDeviceReset
+// created a new primary context, which may place the array elsewhere)
+// looks it up again.  The first call in a context should come before any
+// stream capture begins.
 // Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library
 // routine.
 //
@@ -26,7 +26,8 @@
 // zero; but two calls whose kernels overlap on the GPU (different streams
 // without ordering, or two host threads on different streams) race on the
 // buffer and give wrong results.  Order such calls on one stream.
-#include <atomic>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <mutex>
 
 #include "gconv_internal.h"
@@ -39,24 +40,52 @@ constexpr uint64_t kWgradStaticBytes = 8ull << 20;   // 8 MiB per device
 __device__ __align__(256) unsigned char g_wgrad_scratch[kWgradStaticBytes];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void *> g_scratch_addr[kMaxDevices];
+
+// cuCtxGetCurrent, resolved once through the runtime (the library does not
+// link the driver library).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    });
+    return fn;
+}
+
+struct ScratchEntry {
+    void *ctx = nullptr;    // the context the address was looked up in
+    void *addr = nullptr;
+};
+ScratchEntry g_scratch[kMaxDevices];
 std::mutex g_scratch_mutex;
 
-// The buffer's device address on the current device (looked up once).
+// The buffer's device address in the current context.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        std::lock_guard<std::mutex> lock(g_scratch_mutex);
-        p = g_scratch_addr[dev].load(std::memory_order_acquire);
-        if (p == nullptr) {
-            e = cudaGetSymbolAddress(&p, g_wgrad_scratch);
-            if (e != cudaSuccess) return e;
-            g_scratch_addr[dev].store(p, std::memory_order_release);
-        }
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn fn = ctx_get_current();
+    const bool have_ctx = fn && fn(&ctx) == CUDA_SUCCESS && ctx != nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    ScratchEntry &en = g_scratch[dev];
+    if (have_ctx && en.addr && en.ctx == (void *)ctx) {
+        *out = en.addr;
+        return cudaSuccess;
+    }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_wgrad_scratch);
+    if (e != cudaSuccess) return e;
+    if (have_ctx) {
+        en.ctx = (void *)ctx;
+        en.addr = p;
     }
     *out = p;
     return cudaSuccess;
