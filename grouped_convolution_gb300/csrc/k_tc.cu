@@ -426,8 +426,11 @@ tc_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *__restrict_
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        f[e] = bad ? __int_as_float(0x7fc00000)
-                                   : __uint_as_float(v[nb][e]) + bias_s[buf * 32 + nb * 8 + e];
+                        f[e] = __uint_as_float(v[nb][e]) + bias_s[buf * 32 + nb * 8 + e];
+                    if (bad) {   // a failed CTA writes NaN
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = __int_as_float(0x7fc00000);
+                    }
                     if (g.vec_store) {
                         uint4 o;
                         o.x = pack2(f[0], f[1], (T *)nullptr);
