@@ -42,6 +42,10 @@ struct Schedule {
     cudaError_t (*launch)(const Params &pr, const Ptrs &p, cudaStream_t s, int *launches);
 };
 
+// Programmatic dependent launch for the library's kernels: GCONV_PDL=1 in
+// the environment (read once).
+bool pdl_enabled();
+
 // Schedules, indexed by gconv_schedule.
 extern const Schedule kDwFlat;
 extern const Schedule kDwRow8;

@@ -33,6 +33,20 @@ thread_local int32_t t_last_cuda_error = 0;
 const Schedule *const kSchedules[GCONV_SCHED_COUNT] = {
     &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc, &kDwLine, &kDwSmall, &kDwTc};
 
+}  // namespace
+
+namespace gconv {
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("GCONV_PDL");
+        return e && e[0] == '1' && e[1] == 0;
+    }();
+    return on;
+}
+}  // namespace gconv
+
+namespace {
+
 int32_t schedule_from_string(const char *s) {
     if (!s || !*s) return GCONV_SCHED_AUTO;
     if (!strcmp(s, "auto")) return GCONV_SCHED_AUTO;

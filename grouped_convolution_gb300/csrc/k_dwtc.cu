@@ -411,7 +411,7 @@ cudaError_t dwtc_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const 
     cudaError_t e =
         cudaFuncSetAttribute(dwtc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(dwtc_kernel<T>, dim3(g.ctas), dim3(kDThreads), g.smem, s, map,
+    e = launch_kernel(dwtc_kernel<T>, dim3(g.ctas), dim3(kDThreads), g.smem, s, map,
                    static_cast<const T *>(q.w), static_cast<const T *>(q.b),
                    static_cast<T *>(q.y), p, g);
     return e != cudaSuccess ? e : cudaGetLastError();

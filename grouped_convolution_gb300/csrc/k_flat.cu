@@ -83,14 +83,14 @@ cudaError_t flat_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *lau
         cudaError_t e;
         const bool small = total <= INT32_MAX;
         if (p.transposed)
-            e = small ? launch_pdl(flat_kernel<T, int, true>, dim3((unsigned)blocks), dim3(threads),
+            e = small ? launch_kernel(flat_kernel<T, int, true>, dim3((unsigned)blocks), dim3(threads),
                                    0, s, x, w, b, y, p, total)
-                      : launch_pdl(flat_kernel<T, int64_t, true>, dim3((unsigned)blocks),
+                      : launch_kernel(flat_kernel<T, int64_t, true>, dim3((unsigned)blocks),
                                    dim3(threads), 0, s, x, w, b, y, p, total);
         else
-            e = small ? launch_pdl(flat_kernel<T, int, false>, dim3((unsigned)blocks),
+            e = small ? launch_kernel(flat_kernel<T, int, false>, dim3((unsigned)blocks),
                                    dim3(threads), 0, s, x, w, b, y, p, total)
-                      : launch_pdl(flat_kernel<T, int64_t, false>, dim3((unsigned)blocks),
+                      : launch_kernel(flat_kernel<T, int64_t, false>, dim3((unsigned)blocks),
                                    dim3(threads), 0, s, x, w, b, y, p, total);
         (void)per_image;
         *launches = 1;

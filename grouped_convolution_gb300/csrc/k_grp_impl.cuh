@@ -12,7 +12,7 @@ cudaError_t grp_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const G
     cudaError_t e = cudaFuncSetAttribute(grp_kernel<T, CIP, MB, SW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(grp_kernel<T, CIP, MB, SW>, dim3((unsigned)g.tiles), dim3(kGrpThreads), smem, s,
+    e = launch_kernel(grp_kernel<T, CIP, MB, SW>, dim3((unsigned)g.tiles), dim3(kGrpThreads), smem, s,
                    static_cast<const T *>(q.x), static_cast<const T *>(q.w),
                    static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
     return e != cudaSuccess ? e : cudaGetLastError();

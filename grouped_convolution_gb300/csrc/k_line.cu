@@ -394,7 +394,7 @@ cudaError_t line_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *lau
             const int64_t need = (g.items + g.PB - 1) / g.PB;
             if (bx > need) bx = need;
             if (bx > INT32_MAX) bx = INT32_MAX;
-            e = launch_pdl(kernel, dim3((unsigned)bx, (unsigned)chunks), dim3(g.CVb * g.PB), smem,
+            e = launch_kernel(kernel, dim3((unsigned)bx, (unsigned)chunks), dim3(g.CVb * g.PB), smem,
                            s, static_cast<const T *>(q.x), static_cast<const T *>(q.w),
                            static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
             return e != cudaSuccess ? e : cudaGetLastError();

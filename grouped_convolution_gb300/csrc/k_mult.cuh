@@ -446,7 +446,7 @@ cudaError_t mult_launch_t(const CUtensorMap &map, const Params &p, const Ptrs &q
     cudaError_t e = cudaFuncSetAttribute(mult_kernel<T, SW, MB, KWT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(mult_kernel<T, SW, MB, KWT>, dim3(g.ctas), dim3(kMultThreads), g.smem, s, map,
+    e = launch_kernel(mult_kernel<T, SW, MB, KWT>, dim3(g.ctas), dim3(kMultThreads), g.smem, s, map,
                    static_cast<const T *>(q.x), static_cast<const T *>(q.w),
                    static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
     return e != cudaSuccess ? e : cudaGetLastError();

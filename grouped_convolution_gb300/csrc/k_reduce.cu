@@ -96,7 +96,7 @@ cudaError_t reduce_launch(const Params &p, const Ptrs &q, cudaStream_t s, int *l
         T *y = static_cast<T *>(q.y);
         cudaError_t e;
         auto go = [&](auto kernel) {
-            return launch_pdl(kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0, s, x, w, b,
+            return launch_kernel(kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0, s, x, w, b,
                               y, p, total);
         };
         if (p.transposed)

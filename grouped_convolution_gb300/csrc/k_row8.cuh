@@ -459,7 +459,7 @@ cudaError_t row8_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(row8_kernel<T, K, SH, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(row8_kernel<T, K, SH, D>, dim3(g.ctas), dim3(g.CVc * g.PG), smem, s, map,
+    e = launch_kernel(row8_kernel<T, K, SH, D>, dim3(g.ctas), dim3(g.CVc * g.PG), smem, s, map,
                    static_cast<const T *>(q.x), static_cast<const T *>(q.w),
                    static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
     return e != cudaSuccess ? e : cudaGetLastError();

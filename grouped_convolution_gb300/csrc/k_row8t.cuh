@@ -354,7 +354,7 @@ cudaError_t row8t_launch_t(const Params &p, const Ptrs &q, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(row8t_kernel<T, K>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(row8t_kernel<T, K>, dim3(g.ctas), dim3(g.CVc * g.PG), smem, s, map,
+    e = launch_kernel(row8t_kernel<T, K>, dim3(g.ctas), dim3(g.CVc * g.PG), smem, s, map,
                    static_cast<const T *>(q.w), static_cast<const T *>(q.b),
                    static_cast<T *>(q.y), p, g);
     return e != cudaSuccess ? e : cudaGetLastError();

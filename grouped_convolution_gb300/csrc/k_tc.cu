@@ -524,7 +524,7 @@ cudaError_t tc_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const Tc
     cudaError_t e = cudaFuncSetAttribute(tc_kernel<T, SW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(tc_kernel<T, SW>, dim3(g.ctas), dim3(kTcThreads), smem, s,
+    e = launch_kernel(tc_kernel<T, SW>, dim3(g.ctas), dim3(kTcThreads), smem, s,
                    static_cast<const T *>(q.x), static_cast<const T *>(q.w),
                    static_cast<const T *>(q.b), static_cast<T *>(q.y), p, g);
     return e != cudaSuccess ? e : cudaGetLastError();

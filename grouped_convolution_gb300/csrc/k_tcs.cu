@@ -584,14 +584,14 @@ cudaError_t tcs_launch_t(const Params &p, const Ptrs &q, cudaStream_t s, const T
         e = cudaFuncSetAttribute(tcs_kernel<T, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  g.smem);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(tcs_kernel<T, 16>, dim3(g.ctas), dim3(kSThreads), g.smem, s, map,
+        e = launch_kernel(tcs_kernel<T, 16>, dim3(g.ctas), dim3(kSThreads), g.smem, s, map,
                        static_cast<const T *>(q.w), static_cast<const T *>(q.b),
                        static_cast<T *>(q.y), p, g);
     } else {
         e = cudaFuncSetAttribute(tcs_kernel<T, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  g.smem);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(tcs_kernel<T, 8>, dim3(g.ctas), dim3(kSThreads), g.smem, s, map,
+        e = launch_kernel(tcs_kernel<T, 8>, dim3(g.ctas), dim3(kSThreads), g.smem, s, map,
                        static_cast<const T *>(q.w), static_cast<const T *>(q.b),
                        static_cast<T *>(q.y), p, g);
     }

@@ -568,7 +568,7 @@ template <typename T, int TMAX>
 cudaError_t launch_cl(const Params &p, const T *x, const T *gy, float *ws, const WgPlan &pl,
                       cudaStream_t s) {
     constexpr int CH = wg_ch<T, TMAX>();
-    return launch_pdl(wgrad_cl_kernel<T, TMAX, CH>, dim3(pl.slices, pl.chunks),
+    return launch_kernel(wgrad_cl_kernel<T, TMAX, CH>, dim3(pl.slices, pl.chunks),
                       dim3(pl.CVb * pl.PL), 0, s, x, gy, ws, p, pl);
 }
 
@@ -579,7 +579,7 @@ cudaError_t finish_launch(const Params &p, const float *ws, void *dw, void *db, 
     const int64_t blocks = (total + kFinEntries - 1) / kFinEntries;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     return GCONV_DISPATCH_DTYPE(p.dtype, T, [&] {
-        cudaError_t e = launch_pdl(wgrad_finish_kernel<T>, dim3((unsigned)blocks),
+        cudaError_t e = launch_kernel(wgrad_finish_kernel<T>, dim3((unsigned)blocks),
                                    dim3(kFinEntries * kFinGroups), 0, s, ws,
                                    static_cast<T *>(dw), static_cast<T *>(db), p.C_out, T1, slices);
         return e != cudaSuccess ? e : cudaGetLastError();
@@ -631,20 +631,20 @@ cudaError_t wgrad_launch(const Params &p, const void *x, const void *gy, void *d
         cudaError_t e;
         const dim3 sg(pl.slices, pl.chunks), sb(pl.CVb * pl.PL);
         if (sk == 33) {
-            e = launch_pdl(wgrad_strip_kernel<T, 3, 3, 1>, sg, sb, 0, s, xt, gt, ws, p, pl);
+            e = launch_kernel(wgrad_strip_kernel<T, 3, 3, 1>, sg, sb, 0, s, xt, gt, ws, p, pl);
         } else if (sk == 19) {
-            e = launch_pdl(wgrad_strip_kernel<T, 1, 9, 1>, sg, sb, 0, s, xt, gt, ws, p, pl);
+            e = launch_kernel(wgrad_strip_kernel<T, 1, 9, 1>, sg, sb, 0, s, xt, gt, ws, p, pl);
         } else if (sk == 233) {
-            e = launch_pdl(wgrad_strip_kernel<T, 3, 3, 2>, sg, sb, 0, s, xt, gt, ws, p, pl);
+            e = launch_kernel(wgrad_strip_kernel<T, 3, 3, 2>, sg, sb, 0, s, xt, gt, ws, p, pl);
         } else if (sk == 219) {
-            e = launch_pdl(wgrad_strip_kernel<T, 1, 9, 2>, sg, sb, 0, s, xt, gt, ws, p, pl);
+            e = launch_kernel(wgrad_strip_kernel<T, 1, 9, 2>, sg, sb, 0, s, xt, gt, ws, p, pl);
         } else if (cl) {
             if (pl.tmax == 9) e = launch_cl<T, 9>(p, xt, gt, ws, pl, s);
             else if (pl.tmax == 25) e = launch_cl<T, 25>(p, xt, gt, ws, pl, s);
             else e = launch_cl<T, 49>(p, xt, gt, ws, pl, s);
         } else {
             const int gy_blocks = p.C_out < 65535 ? p.C_out : 65535;
-            e = launch_pdl(wgrad_generic_kernel<T>, dim3(pl.slices, gy_blocks), dim3(kWgThreads), 0,
+            e = launch_kernel(wgrad_generic_kernel<T>, dim3(pl.slices, gy_blocks), dim3(kWgThreads), 0,
                            s, xt, gt, ws, p, pl);
         }
         if (e != cudaSuccess) return e;

@@ -280,7 +280,7 @@ cudaError_t wrow_launch_t(const Params &p, const void *x, const void *gy, float 
     cudaError_t e = cudaFuncSetAttribute(wgrad_row_kernel<T, K, SH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(wgrad_row_kernel<T, K, SH>, dim3(wg.ctas, g.HC), dim3(g.CVc * g.PG), smem, s,
+    e = launch_kernel(wgrad_row_kernel<T, K, SH>, dim3(wg.ctas, g.HC), dim3(g.CVc * g.PG), smem, s,
                    xmap, gmap, ws, p, wg);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
