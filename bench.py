@@ -214,6 +214,7 @@ KERNEL_SOURCES = {
     "dw_flat": ["k_flat.cu", "device_common.cuh", "launch.cuh"],
     "dw_small": ["k_small.cu", "device_common.cuh", "launch.cuh"],
     "dw_tc": ["k_dwtc.cu", "tc_common.cuh", "device_common.cuh", "tma.cuh", "tma.cu", "launch.cuh"],
+    "dw_tcl": ["k_dwtcl.cu", "tc_common.cuh", "device_common.cuh", "tma.cuh", "tma.cu", "launch.cuh"],
     "dw_mult": ["k_mult.cuh", "k_mult.cu", "device_common.cuh", "tma.cuh", "launch.cuh"],
     "grp_plane": ["k_grp.cuh", "k_grp_impl.cuh", "k_grp.cu", "device_common.cuh", "launch.cuh"],
     "grp_reduce": ["k_reduce.cu", "device_common.cuh", "launch.cuh"],

@@ -37,7 +37,8 @@ __all__ = [
 ]
 
 SCHEDULES = {"auto": -1, "dw_flat": 0, "dw_row8": 1, "dw_mult": 2,
-             "grp_plane": 3, "grp_reduce": 4, "grp_tc": 5, "dw_line": 6, "dw_small": 7, "dw_tc": 8}
+             "grp_plane": 3, "grp_reduce": 4, "grp_tc": 5, "dw_line": 6, "dw_small": 7, "dw_tc": 8,
+             "dw_tcl": 9}
 _DTYPE_CODES = {"float32": 0, "float16": 1, "bfloat16": 2}
 
 _lock = threading.Lock()

@@ -56,6 +56,7 @@ extern const Schedule kGrpTc;
 extern const Schedule kDwLine;
 extern const Schedule kDwSmall;
 extern const Schedule kDwTc;
+extern const Schedule kDwTcl;
 
 // The plain forward convolution of the direct-stencil envelope (dilation 1,
 // not transposed): the only calls the specialised schedules take.

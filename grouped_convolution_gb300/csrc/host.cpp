@@ -31,7 +31,7 @@ std::atomic<uint64_t> g_launches{0};
 thread_local int32_t t_last_cuda_error = 0;
 
 const Schedule *const kSchedules[GCONV_SCHED_COUNT] = {
-    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc, &kDwLine, &kDwSmall, &kDwTc};
+    &kDwFlat, &kDwRow8, &kDwMult, &kGrpPlane, &kGrpReduce, &kGrpTc, &kDwLine, &kDwSmall, &kDwTc, &kDwTcl};
 
 }  // namespace
 

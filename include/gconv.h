@@ -138,7 +138,11 @@ typedef enum gconv_schedule {
                                     at stride 1: input rows times banded weight matrices on
                                     the tcgen05 tensor cores, fp32 accumulation in tensor
                                     memory */
-    GCONV_SCHED_COUNT = 9
+    GCONV_SCHED_DW_TCL = 9,      /* channels-last bf16 / fp16 depthwise (multiplier 1) at
+                                    stride 1, channels a multiple of 8: the input transposed
+                                    to channel planes in shared memory, rows times banded
+                                    weight matrices on the tcgen05 tensor cores */
+    GCONV_SCHED_COUNT = 10
 } gconv_schedule;
 
 typedef enum gconv_layout {

@@ -61,8 +61,11 @@ def test_header_compiles_as_c(tmp_path):
 def test_version_and_names(libpath):
     gc.build()
     assert gc._load().conv_version() >= 100
-    assert [gc.conv_schedule_name(i) for i in range(6)] == [
-        "dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc"]
+    assert [gc.conv_schedule_name(i) for i in range(10)] == [
+        "dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc", "dw_line",
+        "dw_small", "dw_tc", "dw_tcl"]
+    assert {gc.conv_schedule_name(i): i for i in range(10)} == {
+        k: v for k, v in gc.SCHEDULES.items() if k != "auto"}
     assert gc.conv_schedule_name(-1) == "auto"
     assert gc.conv_schedule_name(99) == "unknown"
     assert gc.conv_strerror(0) == "ok"

@@ -206,7 +206,7 @@ def test_force_schedule_rules():
     assert status_of(lambda: gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE)) == ERR["SCHEDULE"]
     d.schedule = gc.SCHEDULES["dw_row8"]      # depthwise-only schedule on a grouped call
     assert status_of(lambda: gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE)) == ERR["SCHEDULE"]
-    assert status_of(lambda: gc.conv_force_schedule(9)) == ERR["SCHEDULE"]
+    assert status_of(lambda: gc.conv_force_schedule(len(gc.SCHEDULES) - 1)) == ERR["SCHEDULE"]
     gc.conv_force_schedule("dw_flat")
     d.schedule = -1
     assert gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE) == "dw_flat"

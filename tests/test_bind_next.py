@@ -148,7 +148,7 @@ def test_schedule_selection_wider_envelope():
     d = gc.conv_bind(dense((8, 64, 20, 20)), dense((64, 1, 3, 3)), None, 1, 2, 2, 2, 64,
                      dtype="bfloat16")
     assert select(d) == "dw_small"
-    for s in ("dw_row8", "dw_mult", "grp_plane", "grp_tc", "dw_tc"):
+    for s in ("dw_row8", "dw_mult", "grp_plane", "grp_tc", "dw_tc", "dw_tcl"):
         d.schedule = gc.SCHEDULES[s]
         assert status_of(lambda: select(d)) == ERR["SCHEDULE"]
     # 1-D channels-last depthwise -> dw_line

@@ -49,7 +49,8 @@ GEOMS = [
 ]
 
 DTYPES = ["f32", "f16", "bf16"]
-SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc", "dw_small", "dw_tc"]
+SCHED = ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce", "grp_tc", "dw_small", "dw_tc",
+         "dw_tcl"]
 
 
 def workload(g, dtype, cl, bias, seed):
@@ -218,6 +219,41 @@ def test_dw_tc_geometry_matches_oracle(case, dtype):
     y = run_gpu(wl, x, w, b, "dw_tc")
     assert y is not None, "dw_tc must take this case"
     RAN["dw_tc"] += 1
+    check(wl, x, w, b, y)
+
+
+# dw_tcl (channels-last 16-bit depthwise at stride 1 on the tensor cores)
+# geometry: several short images stacked in one 128-row tile (a full stack
+# and a partial one), images taller than a tile (row blocks), kernels 1x1 to
+# 9x9 and 2x8 with every column-tile width, ragged last column tiles,
+# asymmetric padding, one channel group per CTA and (past 152 groups) many.
+DWTCL_CASES = [
+    # name, N, Cin_g, Cout_g, G, H, W, KH, KW, stride, pad_before, pad_after
+    # (channels-last, channels a multiple of 8: the input arrives as TMA boxes
+    # of 8 channels)
+    ("two_images_per_tile", 4, 1, 1, 16, 56, 56, 7, 7, (1, 1), (3, 3), (3, 3)),
+    ("row_blocks", 1, 1, 1, 16, 130, 21, 5, 5, (1, 1), (2, 2), (2, 2)),
+    ("partial_stack", 5, 1, 1, 8, 9, 40, 7, 7, (1, 1), (3, 3), (3, 3)),
+    ("asym_4x6", 2, 1, 1, 24, 17, 30, 4, 6, (1, 1), (1, 2), (2, 3)),
+    ("k9_three_blocks", 1, 1, 1, 8, 300, 9, 9, 9, (1, 1), (4, 4), (4, 4)),
+    ("k1", 3, 1, 1, 8, 11, 33, 1, 1, (1, 1), (0, 0), (0, 0)),
+    ("k2x8_pad7", 2, 1, 1, 8, 64, 19, 2, 8, (1, 1), (0, 7), (1, 0)),
+    ("many_groups", 2, 1, 1, 96, 20, 20, 3, 3, (1, 1), (1, 1), (1, 1)),
+    ("c96_56x56", 6, 1, 1, 96, 56, 56, 7, 7, (1, 1), (3, 3), (3, 3)),
+    # more channel groups than SMs: one contiguous split of all units
+    ("groups_past_sm_count", 1, 1, 1, 1232, 9, 12, 3, 3, (1, 1), (1, 1), (1, 1)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("case", DWTCL_CASES, ids=[c[0] for c in DWTCL_CASES])
+def test_dw_tcl_geometry_matches_oracle(case, dtype):
+    i = DWTCL_CASES.index(case)
+    wl = workload(case, dtype, True, i % 2 == 0, seed=131 + i)
+    x, w, b = make_inputs(wl)
+    y = run_gpu(wl, x, w, b, "dw_tcl")
+    assert y is not None, "dw_tcl must take this case"
+    RAN["dw_tcl"] += 1
     check(wl, x, w, b, y)
 
 

@@ -49,7 +49,8 @@ def test_full_size_workload(name):
 
 
 @pytest.mark.parametrize("schedule", ["dw_flat", "dw_row8", "dw_mult", "grp_plane", "grp_reduce",
-                                      "grp_tc", "dw_line", "dw_small", "dw_tc"])
+                                      "grp_tc", "dw_line", "dw_small", "dw_tc",
+                                      "dw_tcl"])
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_reduced_workload_every_schedule(name, schedule):
     wl = small_variant(WORKLOADS[name], N=2, H=min(WORKLOADS[name].H, 29),
