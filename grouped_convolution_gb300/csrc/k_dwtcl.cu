@@ -329,30 +329,35 @@ dwtcl_kernel(const T *__restrict__ x, const T *__restrict__ w,
         const int tw = warp - kLWTrans, tt = t - 32 * kLWTrans;
         // Channel group cg's banded matrices: block (c, kh) is a 16 x 16
         // K-major matrix whose row j holds at K = k the weight at kernel
-        // column k - j (zero outside the kernel and for rows j >= OWC).
+        // column k - j (zero outside the kernel and for rows j >= OWC).  A
+        // thread builds whole blocks: its KW weights load at once (the loads
+        // overlap), and each row is the previous one shifted by a column.
         auto stage_b = [&](int cg) {
             unsigned char *bsm = l_smem + g.b_off;
-            const int rows = 8 * p.KH * 16;
-            for (int row = tt; row < rows; row += kLTransThreads) {
-                const int blk = row >> 4, j = row & 15;
+            for (int blk = tt; blk < 8 * p.KH; blk += kLTransThreads) {
                 const int c = blk / p.KH, kh = blk - c * p.KH;
                 const T *wr = w + (int64_t)(8 * cg + c) * p.ws[0] + (int64_t)kh * p.ws[2];
-                unsigned char *dst = bsm + blk * 512 + (j >> 3) * 256 + (j & 7) * 16;
+                float row[16];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float v[8];
+                for (int k = 0; k < 16; ++k)
+                    row[k] = (k < 9 && k < p.KW) ? load_f32(wr + (int64_t)k * p.ws[3]) : 0.f;
+                unsigned char *dst = bsm + blk * 512;
+#pragma unroll 1
+                for (int j = 0; j < 16; ++j) {
+                    const float on = j < g.owc ? 1.f : 0.f;
+                    uint4 o[2];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int kw = 8 * h + e - j;
-                        v[e] = (j < g.owc && kw >= 0 && kw < p.KW) ? load_f32(wr + (int64_t)kw * p.ws[3])
-                                                                   : 0.f;
+                    for (int h = 0; h < 2; ++h) {
+                        o[h].x = pack2(on * row[8 * h + 0], on * row[8 * h + 1], (T *)nullptr);
+                        o[h].y = pack2(on * row[8 * h + 2], on * row[8 * h + 3], (T *)nullptr);
+                        o[h].z = pack2(on * row[8 * h + 4], on * row[8 * h + 5], (T *)nullptr);
+                        o[h].w = pack2(on * row[8 * h + 6], on * row[8 * h + 7], (T *)nullptr);
                     }
-                    uint4 o;
-                    o.x = pack2(v[0], v[1], (T *)nullptr);
-                    o.y = pack2(v[2], v[3], (T *)nullptr);
-                    o.z = pack2(v[4], v[5], (T *)nullptr);
-                    o.w = pack2(v[6], v[7], (T *)nullptr);
-                    *reinterpret_cast<uint4 *>(dst + h * 128) = o;
+                    *reinterpret_cast<uint4 *>(dst + (j >> 3) * 256 + (j & 7) * 16) = o[0];
+                    *reinterpret_cast<uint4 *>(dst + (j >> 3) * 256 + (j & 7) * 16 + 128) = o[1];
+#pragma unroll
+                    for (int k = 15; k > 0; --k) row[k] = row[k - 1];
+                    row[0] = 0.f;
                 }
             }
         };
