@@ -242,6 +242,43 @@ def test_dw_small_takes_depthwise_only():
     assert status_of(lambda: gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE)) == ERR["SCHEDULE"]
 
 
+def test_dw_tcl_support_rules():
+    """dw_tcl takes channels-last 16-bit depthwise calls (multiplier 1) at
+    stride 1 and dilation 1 with channels in groups of 8, and nothing else;
+    a misaligned input is an alignment error, not a silent fallback."""
+    def cl(N, C, H, W, K=3, groups=None, dtype="bfloat16", stride=1, dil=1, cout=None, pad=1):
+        cout = cout or C
+        return bind(x=((N, C, H, W), cl_strides(N, C, H, W)),
+                    w=((cout, C // (groups or C), K, K), None), groups=groups or C,
+                    stride=stride, pb=pad, dil=dil, dtype=dtype)
+
+    def forced(d, x=FAKE):
+        d.schedule = gc.SCHEDULES["dw_tcl"]
+        return status_of(lambda: gc.conv_select_schedule(d, x, FAKE, None, FAKE))
+
+    for dtype in ("bfloat16", "float16"):
+        for K in (1, 3, 7, 9):
+            assert forced(cl(2, 96, 56, 56, K=K, pad=K // 2, dtype=dtype)) == 0, (dtype, K)
+    assert forced(cl(1, 8, 300, 9, K=9, pad=4)) == 0           # taller than a 128-row tile
+    assert forced(cl(1, 1232, 9, 12)) == 0                      # more channel groups than SMs
+    refused = [
+        cl(2, 96, 56, 56, dtype="float32"),                     # fp32
+        cl(2, 12, 20, 20),                                      # channels not a multiple of 8
+        cl(2, 96, 20, 20, stride=2),                            # stride 2
+        cl(2, 96, 20, 20, dil=2, pad=2),                        # dilation 2
+        cl(2, 96, 20, 20, cout=192),                            # multiplier 2
+        cl(2, 96, 20, 20, groups=48),                           # two channels per group
+        bind(x=((2, 96, 20, 20), None), w=((96, 1, 3, 3), None), groups=96,
+             dtype="bfloat16"),                                 # NCHW
+    ]
+    for d in refused:
+        assert forced(d) == ERR["SCHEDULE"], (d.C_in, d.stride[0], d.dilation[0], d.layout)
+    assert forced(cl(2, 96, 20, 20), x=FAKE + 2) == ERR["ALIGN"]
+    # not the picker's choice for the benchmark's 7x7 layer (dw_row8 is)
+    d = cl(128, 96, 56, 56, K=7, pad=3)
+    assert gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE) == "dw_row8"
+
+
 def test_dw_forward_refuses_grouped():
     d = bind(x=((1, 8, 8, 8), None), w=((8, 2, 3, 3), None), groups=4)
     assert status_of(lambda: gc.conv_dw_forward(d, FAKE, FAKE, None, FAKE, 0)) == ERR["UNSUPPORTED"]
