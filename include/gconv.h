@@ -107,10 +107,12 @@ typedef enum gconv_status {
 } gconv_status;
 
 /* The five schedules of the direct-stencil template (PR #25085, second
- * paragraph), re-designed for sm_103a, plus a tensor-core schedule for
- * 4- and 8-channel groups and a channels-last depthwise schedule for the
- * shapes outside the others' reach (dilated, 1-D, non-square, transposed).
- * GCONV_SCHED_AUTO lets the per-shape picker choose. */
+ * paragraph), re-designed for sm_103a, plus: a tensor-core schedule for
+ * 4- and 8-channel groups; a channels-last depthwise schedule for the
+ * shapes outside the others' reach (dilated, 1-D, non-square, transposed);
+ * a one-wave schedule for small depthwise problems; and two tensor-core
+ * depthwise schedules (banded weight matrices) for NCHW and channels-last
+ * 16-bit tensors.  GCONV_SCHED_AUTO lets the per-shape picker choose. */
 typedef enum gconv_schedule {
     GCONV_SCHED_AUTO = -1,
     GCONV_SCHED_DW_FLAT = 0,     /* fallback: any layout, multiplier and group shape */
