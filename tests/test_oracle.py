@@ -16,6 +16,7 @@ executorch PR #25084, description.
 """
 
 import itertools
+import os
 
 import numpy as np
 import pytest
@@ -357,3 +358,60 @@ def test_tolerance_rule():
     got = np.array([1.0 + 6.85e-4, 1.0 + 6.95e-4, 5e-7])
     assert list(oracle.violations(got, ref, bound, "f16")) == [False, True, False]
     assert oracle.violations(np.array([np.nan]), np.array([0.0]), np.array([1.0]), "f32")[0]
+
+
+# ------------------------------------------------------------ golden fixtures
+# tests/golden/*.txt hold tiny integer-valued cases written by
+# tests/golden/make_golden.py from this oracle (the pages print no worked
+# values).  They guard the oracle against silent change; the box-sum case is
+# also checked against a closed form computed another way (a summed-area
+# table), not by re-running the stencil.
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(path):
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, _, rest = line.strip().partition(" ")
+            fields[key] = rest
+    ints = lambda k: tuple(int(v) for v in fields[k].split())
+    arr = lambda k, shape: np.array([float(v) for v in fields[k].split()]).reshape(shape)
+    return {
+        "x": arr("x", ints("x_shape")), "w": arr("w", ints("w_shape")),
+        "b": None if fields["b"] == "none" else np.array([float(v) for v in fields["b"].split()]),
+        "y": arr("y", ints("y_shape")), "stride": ints("stride"), "pb": ints("pad_before"),
+        "pa": ints("pad_after"), "groups": int(fields["groups"]), "dilation": ints("dilation"),
+    }
+
+
+GOLDEN_NAMES = sorted(f[:-4] for f in os.listdir(GOLDEN) if f.endswith(".txt"))
+
+
+def test_golden_fixtures_exist():
+    assert len(GOLDEN_NAMES) >= 4
+
+
+@pytest.mark.parametrize("name", GOLDEN_NAMES)
+def test_golden_fixture_reproduced(name):
+    g = _read_golden(os.path.join(GOLDEN, name + ".txt"))
+    y, bound = oracle.conv2d(g["x"], g["w"], g["b"], g["stride"], g["pb"], g["pa"], g["groups"],
+                             g["dilation"])
+    assert y.shape == g["y"].shape
+    assert np.array_equal(y, g["y"])          # integer inputs: exact
+    assert (bound >= np.abs(y - (0 if g["b"] is None else g["b"][None, :, None, None]))).all()
+
+
+def test_golden_box_sums_match_summed_area_table():
+    g = _read_golden(os.path.join(GOLDEN, "box3x3_ramp4x4.txt"))
+    x = g["x"][0, 0]
+    xp = np.pad(x, 1)
+    S = np.zeros((xp.shape[0] + 1, xp.shape[1] + 1))
+    S[1:, 1:] = xp.cumsum(0).cumsum(1)
+    H, W = x.shape
+    want = np.array([[S[i + 3, j + 3] - S[i, j + 3] - S[i + 3, j] + S[i, j] for j in range(W)]
+                     for i in range(H)])
+    assert np.array_equal(g["y"][0, 0], want)
