@@ -23,11 +23,14 @@
 //  - A unit is one channel group of 8 channels, one stack of segments and
 //    one column tile.  Its input (8 channels x 16 columns x P rows per
 //    segment) is copied into a ring slot as 16-byte pieces, one per pixel,
-//    by asynchronous copies from the loader warp's lanes (cp.async with a
-//    zero source size for the padding), which an mbarrier tracks.  A
-//    16-byte piece every 2 C bytes is where the copy engine is slow (a box
-//    of such pieces ran at about 0.16 pieces per cycle per SM); the
-//    load/store path takes them at the rate of its cache-line requests.
+//    by asynchronous copies from three warps (cp.async with a zero source
+//    size for the padding), which an mbarrier tracks.  A 16-byte piece
+//    every 2 C bytes is where the copy engine is slow (a box of such pieces
+//    ran at about 0.16 pieces per cycle per SM); the load/store path takes
+//    them at the rate of its cache-line requests, and one warp alone could
+//    not issue them fast enough.  CTA i keeps channel group i mod (C / 8):
+//    the groups' pieces of one pixel reach L2 at about the same time, from
+//    sibling CTAs working through the same spatial units.
 //    Two transposing warps turn each staged row
 //    into the MMA operand: an ldmatrix of 8 pixels x 8 channels and a
 //    transposing stmatrix give each channel's 8 consecutive columns as one
