@@ -433,6 +433,17 @@ static int32_t pick(const gconv_desc &d, const Ptrs &p) {
         (double)d.N * d.C_out * d.OH * d.OW <= (double)(1 << 20) && kDwSmall.supports(d, p))
         return GCONV_SCHED_DW_SMALL;
     if (dw && d.Cout_g == 1 && kDwRow8.supports(d, p)) return GCONV_SCHED_DW_ROW8;
+    // Channels-last 16-bit 2-D depthwise layers outside dw_row8's kernels
+    // (even, 9x9 and non-square) at stride 1, with at least 12 taps: the
+    // banded product on the tensor cores.  Measured on N 32, C 96, 56 x 56
+    // bf16: 9x9 35 us against dw_line's 157, 8x8 34 / 130, 3x5 25 / 55,
+    // 5x3 24 / 28, 4x4 25 / 26; but 2x2 23 / 15 and 1x1 23 / 11 (dw_tcl's
+    // copies set a floor the small kernels' arithmetic never reaches).  1-D
+    // layers stay on dw_line: their single rows leave most of a 128-row tile
+    // empty.
+    if (dw && d.Cout_g == 1 && d.spatial_dims == 2 && d.KH * d.KW >= 12 &&
+        kDwTcl.supports(d, p))
+        return GCONV_SCHED_DW_TCL;
     if (dw && kDwTc.supports(d, p)) return GCONV_SCHED_DW_TC;
     if (dw && kDwMult.supports(d, p)) return GCONV_SCHED_DW_MULT;
     if (!dw && kGrpTc.supports(d, p)) return GCONV_SCHED_GRP_TC;

@@ -143,7 +143,8 @@ typedef enum gconv_schedule {
     GCONV_SCHED_DW_TCL = 9,      /* channels-last bf16 / fp16 depthwise (multiplier 1) at
                                     stride 1, channels a multiple of 8: the input transposed
                                     to channel planes in shared memory, rows times banded
-                                    weight matrices on the tcgen05 tensor cores */
+                                    weight matrices on the tcgen05 tensor cores; picked for
+                                    2-D kernels outside dw_row8's with >= 12 taps */
     GCONV_SCHED_COUNT = 10
 } gconv_schedule;
 

@@ -274,9 +274,25 @@ def test_dw_tcl_support_rules():
     for d in refused:
         assert forced(d) == ERR["SCHEDULE"], (d.C_in, d.stride[0], d.dilation[0], d.layout)
     assert forced(cl(2, 96, 20, 20), x=FAKE + 2) == ERR["ALIGN"]
-    # not the picker's choice for the benchmark's 7x7 layer (dw_row8 is)
-    d = cl(128, 96, 56, 56, K=7, pad=3)
-    assert gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE) == "dw_row8"
+    # the picker: dw_row8 keeps its square 3/5/7 kernels (the benchmark's
+    # 7x7 layer among them); other 2-D kernels of >= 12 taps at stride 1 go
+    # to dw_tcl, while small kernels, fp32, dilated and 1-D calls stay on
+    # dw_line
+    pick = lambda d: gc.conv_select_schedule(d, FAKE, FAKE, None, FAKE)
+    assert pick(cl(128, 96, 56, 56, K=7, pad=3)) == "dw_row8"
+    assert pick(cl(8, 64, 20, 20)) == "dw_row8"
+    for K in (4, 6, 8, 9):
+        assert pick(cl(8, 64, 20, 20, K=K, pad=K // 2)) == "dw_tcl", K
+    for K in (1, 2):
+        assert pick(cl(8, 64, 20, 20, K=K, pad=K // 2)) == "dw_line", K
+    nonsquare = bind(x=((8, 64, 20, 20), cl_strides(8, 64, 20, 20)), w=((64, 1, 5, 3), None),
+                     groups=64, pb=(2, 1), dtype="float16")
+    assert pick(nonsquare) == "dw_tcl"
+    assert pick(cl(8, 64, 20, 20, K=4, pad=2, dtype="float32")) == "dw_line"
+    assert pick(cl(8, 64, 20, 20, K=4, pad=3, dil=2)) == "dw_line"
+    d1 = gc.conv1d_bind(((4, 256, 1000), (1000 * 256, 1, 256)), ((256, 1, 4), (4, 4, 1)), None,
+                        1, 3, 0, 1, 256, dtype="bfloat16")
+    assert pick(d1) == "dw_line"
 
 
 def test_dw_forward_refuses_grouped():
