@@ -420,9 +420,12 @@ gconv_status grad_input_shape_and_stride(const gconv_desc *d, int32_t *rank,
 // problems run on dw_small; larger NCHW 16-bit depthwise ones at stride 1 on
 // the tensor cores (dw_tc).  Grouped calls the
 // tensor cores can take (4 or 8 channels per group, channels-last 16-bit)
-// run there.  Channels-last depthwise calls outside dw_row8's reach (1-D,
-// non-square or larger kernels, dilation other than 2 on a stride-1 3x3,
-// transposed calls other than stride 2) run on dw_line.  Other
+// run there.  Channels-last 16-bit 2-D depthwise calls at stride 1 whose
+// kernels dw_row8 does not take run on the tensor cores (dw_tcl) when the
+// kernel has at least 12 taps.  Other channels-last depthwise calls outside
+// dw_row8's reach (1-D, small non-square kernels, fp32, dilation other than
+// 2 on a stride-1 3x3, transposed calls other than stride 2) run on
+// dw_line.  Other
 // calls with too few outputs to give every thread of the GPU its own (fewer
 // than 152 SMs x 512) and a long tap loop split the taps across lanes.
 static int32_t pick(const gconv_desc &d, const Ptrs &p) {
