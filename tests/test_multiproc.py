@@ -64,3 +64,59 @@ def test_reference_arm_under_torchrun_prints_once():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_roofline_bound_rule():
+    """bench.py's roofline: the resource whose peak time is larger bounds a
+    stencil; tensor-core schedules are held to HBM (the FP32 FMA pipe does
+    not do their multiply-adds)."""
+    import types
+    import bench
+    hbm, fma = 6773.5, 39.2e12
+    # FMA-heavy (the 7x7 layer's bytes and FMAs) on an FMA-pipe stencil: alu
+    c = types.SimpleNamespace(bytes=154.15e6, fma=1.888e9, schedule="dw_row8")
+    r = bench.roofline_of(c, 107.3, hbm, fma)
+    assert r["bound"] == "alu" and 0.44 < r["frac"] < 0.46
+    # the same layer on the tensor cores: hbm
+    for s in ("dw_tcl", "dw_tc", "grp_tc"):
+        c.schedule = s
+        r = bench.roofline_of(c, 96.4, hbm, fma)
+        assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+        assert abs(r["achieved"] - 154.15e6 / 96.4e-6 / 1e9) < 0.01
+    # byte-heavy on a stencil: hbm
+    c = types.SimpleNamespace(bytes=57.81e6, fma=0.13e9, schedule="dw_row8")
+    assert bench.roofline_of(c, 17.4, hbm, fma)["bound"] == "hbm"
+
+
+def test_per_config_record_layout(monkeypatch):
+    """bench.py's per-config record, assembled with the GPU parts faked (the
+    case objects and the graph timer): every workload has its entry, the
+    grouped layer carries its direct-stencil timing and the channels-last
+    7x7 layer its tensor-core timing."""
+    import types
+    import bench
+    from grouped_convolution_gb300.inputs import WORKLOADS
+
+    picked = {"grp4x8_9x9_s2_bf16_cl": "grp_tc", "dw4x4_m4_f16_nchw": "dw_tc",
+              "dw3x3_f32_nchw": "dw_small"}
+
+    class FakeCase:
+        def __init__(self, name, sets, dev, schedule=None, *rest):
+            self.schedule = schedule or picked.get(name, "dw_row8")
+            self.bytes, self.fma, self.pix = 100e6, 1e9, 1e6
+
+        def footprint(self):
+            return 1 << 20
+
+    monkeypatch.setattr(bench, "ConvCase", FakeCase)
+    monkeypatch.setattr(bench, "BackwardCase", FakeCase)
+    monkeypatch.setattr(bench, "time_graph", lambda cases, steps, warm, world: (steps * 0.05, None))
+    args = types.SimpleNamespace(steps=20, warmup=3, no_configs=False)
+    out = bench.per_config(args, 1, 126 << 20, 6773.5, 39.2e12, None)
+    for name in WORKLOADS:
+        assert out[name]["us"] == 50.0
+    assert out["grp4x8_9x9_s2_bf16_cl"]["direct_stencil"]["schedule"] == "grp_plane"
+    tc = out["dw7x7_bf16_cl"]["tensor_cores"]
+    assert tc["schedule"] == "dw_tcl" and tc["roofline"]["bound"] == "hbm"
+    assert out["dw7x7_bf16_cl"]["schedule"] == "dw_row8"
+    assert "tensor_cores" not in out["mbv2_dw3x3_s1_bf16_cl"]
